@@ -1,0 +1,195 @@
+"""Python binding of libggufdq (the GB300 GGUF block-dequant GEMV / MoE library).
+
+Argument marshalling only: every function here passes device pointers, sizes and the CUDA
+stream of PyTorch tensors to the C ABI declared in ``include/ggufdq.h`` and raises
+``QGError`` on a non-zero status.  All arithmetic runs in the library's CUDA kernels; there
+is no other code path.  If the shared library has not been built, importing works but the
+first call raises, naming the build step (``gguf_block_dequant_gb300.build.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+Q4_0, Q8_0, Q4_K, Q6_K = 2, 8, 12, 14
+BLOCK = {Q8_0: (32, 34), Q4_0: (32, 18), Q4_K: (256, 144), Q6_K: (256, 210)}
+
+QG_OK, QG_EINVAL_SHAPE, QG_EINVAL_PTR, QG_EALIGN, QG_EUNSUPPORTED, QG_ECUDA, QG_EDEVICE_ID, QG_ETIMEOUT, \
+    QG_EWORKSPACE = range(9)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class QGError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {strerror(status)} (status {status})")
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libggufdq.so (no fallback: raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"{_build.LIB} is not built; run gguf_block_dequant_gb300.build.build()")
+        L = ctypes.CDLL(_build.LIB)
+        P, I, I64, SZ, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+        sig = {
+            "qg_version": ([], I),
+            "qg_strerror": ([I], ctypes.c_char_p),
+            "qg_block_shape": ([I, P, P], I),
+            "qg_device_status": ([P, I], I),
+            "qgemv_q8_0": ([P, P, P, I64, I64, S], I),
+            "qgemv_q4_0": ([P, P, P, I64, I64, S], I),
+            "qgemv_q4_k": ([P, P, P, I64, I64, S], I),
+            "qgemv_q6_k": ([P, P, P, I64, I64, S], I),
+            "qgemv_t": ([I, P, P, P, I64, I64, I, S], I),
+            "qgemm_workspace_size": ([I, I64, I64, I64], SZ),
+            "qgemm": ([I, P, P, P, I64, I64, I64, P, SZ, S], I),
+            "moe_workspace_size": ([I, I, I, I, I], SZ),
+            "moe_route_topk": ([P, P, I, I, I, I, P, P, P, P, SZ, S], I),
+            "moe_expert_swiglu": ([I, P, P, I64, P, I, I, P, P, I, I, I, I, P, P, SZ, S], I),
+            "moe_combine": ([I, P, I64, P, I, I, P, P, P, I, I, I, I, P, I, P, SZ, S], I),
+            "moe_layer": ([I, P, P, P, P, P, I64, P, I, I, I, I, I, I, P, P, P, P, P, SZ, S], I),
+        }
+        for name, (args, res) in sig.items():
+            if hasattr(L, name):
+                f = getattr(L, name)
+                f.argtypes = args
+                f.restype = res
+        _lib = L
+        return L
+
+
+def strerror(status: int) -> str:
+    try:
+        return load().qg_strerror(int(status)).decode()
+    except Exception:  # noqa: BLE001 - message only
+        return f"status {status}"
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _call(name, *args):
+    rc = getattr(load(), name)(*args)
+    if rc != QG_OK:
+        raise QGError(rc, name)
+
+
+def version() -> int:
+    return load().qg_version()
+
+
+def device_status(clear: bool = True) -> int:
+    v = ctypes.c_uint32(0)
+    _call("qg_device_status", ctypes.byref(v), int(clear))
+    return v.value
+
+
+def row_bytes(qtype: int, n: int) -> int:
+    qk, bb = BLOCK[qtype]
+    return (n // qk) * bb
+
+
+# ---- GEMV / GEMM ---------------------------------------------------------------------------
+
+_GEMV1 = {Q8_0: "qgemv_q8_0", Q4_0: "qgemv_q4_0", Q4_K: "qgemv_q4_k", Q6_K: "qgemv_q6_k"}
+
+
+def qgemv(qtype, w, x, M, N, y, stream=None):
+    """y[m] = W[m] . x for one token (qgemv_q8_0 / _q4_0 / _q4_k / _q6_k)."""
+    _call(_GEMV1[qtype], _ptr(w), _ptr(x), _ptr(y), M, N, _stream(stream))
+    return y
+
+
+def qgemv_q8_0(w, x, y, M, N, stream=None):
+    return qgemv(Q8_0, w, x, M, N, y, stream)
+
+
+def qgemv_q4_0(w, x, y, M, N, stream=None):
+    return qgemv(Q4_0, w, x, M, N, y, stream)
+
+
+def qgemv_q4_k(w, x, y, M, N, stream=None):
+    return qgemv(Q4_K, w, x, M, N, y, stream)
+
+
+def qgemv_q6_k(w, x, y, M, N, stream=None):
+    return qgemv(Q6_K, w, x, M, N, y, stream)
+
+
+def qgemv_t(qtype, w, x, y, M, N, T, stream=None):
+    """Y[t][m] = W[m] . X[t] for T <= 16 token rows, one weight pass."""
+    _call("qgemv_t", qtype, _ptr(w), _ptr(x), _ptr(y), M, N, T, _stream(stream))
+    return y
+
+
+def qgemm_workspace_size(qtype, M, N, T) -> int:
+    return int(load().qgemm_workspace_size(qtype, M, N, T))
+
+
+def qgemm(qtype, w, x, y, M, N, T, workspace=None, stream=None):
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _call("qgemm", qtype, _ptr(w), _ptr(x), _ptr(y), M, N, T, _ptr(workspace), ws_bytes, _stream(stream))
+    return y
+
+
+# ---- MoE -------------------------------------------------------------------------------------
+
+def moe_workspace_size(T, k, E, H, F) -> int:
+    return int(load().moe_workspace_size(T, k, E, H, F))
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def moe_route_topk(xn, wr, T, H, E, k, ids, weights, logits=None, workspace=None, stream=None):
+    _call("moe_route_topk", _ptr(xn), _ptr(wr), T, H, E, k, _ptr(ids), _ptr(weights), _ptr(logits),
+          _ptr(workspace), _nbytes(workspace), _stream(stream))
+    return ids, weights
+
+
+def moe_expert_swiglu(qtype, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act,
+                      workspace=None, stream=None):
+    _call("moe_expert_swiglu", qtype, _ptr(w_gate), _ptr(w_up), expert_stride, _ptr(slots), n_slots, E, _ptr(ids),
+          _ptr(xn), T, k, H, F, _ptr(act), _ptr(workspace), _nbytes(workspace), _stream(stream))
+    return act
+
+
+def moe_combine(qtype, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout,
+                add_residual=1, workspace=None, stream=None):
+    _call("moe_combine", qtype, _ptr(w_down), expert_stride, _ptr(slots), n_slots, E, _ptr(ids), _ptr(weights),
+          _ptr(act), T, k, H, F, _ptr(x_inout), int(add_residual), _ptr(workspace), _nbytes(workspace),
+          _stream(stream))
+    return x_inout
+
+
+def moe_layer(qtype, xn, wr, w_gate, w_up, w_down, expert_stride, slots, n_slots, T, H, F, E, k, ids, weights, act,
+              x_inout, workspace=None, stream=None):
+    _call("moe_layer", qtype, _ptr(xn), _ptr(wr), _ptr(w_gate), _ptr(w_up), _ptr(w_down), expert_stride,
+          _ptr(slots), n_slots, T, H, F, E, k, _ptr(ids), _ptr(weights), _ptr(act), _ptr(x_inout),
+          _ptr(workspace), _nbytes(workspace), _stream(stream))
+    return x_inout

@@ -1,0 +1,102 @@
+// qg_abi.cu -- library-wide entry points: version, status strings, block shapes, device
+// status word, and the per-device property cache.
+#include <mutex>
+
+#include "qg_host.h"
+
+namespace qg {
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+std::once_flag g_once[kMaxDevices];
+
+struct AttrEntry {
+  const void *func;
+  int device;
+  uint32_t bytes;
+};
+std::mutex g_attr_mu;
+AttrEntry g_attr[256];
+int g_attr_n = 0;
+}  // namespace
+
+const DeviceInfo &device_info() {
+  static DeviceInfo bad;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return bad;
+  std::call_once(g_once[dev], [dev] {
+    DeviceInfo &d = g_info[dev];
+    d.ok = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+           cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+           cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) == cudaSuccess;
+  });
+  return g_info[dev];
+}
+
+bool set_smem_attr(const void *func, uint32_t bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  for (int i = 0; i < g_attr_n; ++i)
+    if (g_attr[i].func == func && g_attr[i].device == dev) {
+      if (g_attr[i].bytes >= bytes) return true;
+      if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
+          cudaSuccess)
+        return false;
+      g_attr[i].bytes = bytes;
+      return true;
+    }
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) != cudaSuccess)
+    return false;
+  if (g_attr_n < 256) g_attr[g_attr_n++] = AttrEntry{func, dev, bytes};
+  return true;
+}
+
+}  // namespace qg
+
+extern "C" {
+
+int qg_version(void) { return 1; }
+
+const char *qg_strerror(int status) {
+  switch (status) {
+    case QG_OK: return "ok";
+    case QG_EINVAL_SHAPE: return "invalid shape (size out of range or not a multiple of the block size)";
+    case QG_EINVAL_PTR: return "a required pointer is NULL";
+    case QG_EALIGN: return "a pointer or stride is not 16-byte aligned";
+    case QG_EUNSUPPORTED: return "block type or configuration not supported by this call";
+    case QG_ECUDA: return "a CUDA call or kernel launch failed";
+    case QG_EDEVICE_ID: return "device status: an expert id or slot was out of range";
+    case QG_ETIMEOUT: return "device status: a bounded wait inside a kernel expired";
+    case QG_EWORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+qg_status qg_block_shape(int type, int *qk, int *block_bytes) {
+  int a, b;
+  switch (type) {
+    case QG_TYPE_Q8_0: a = 32; b = 34; break;
+    case QG_TYPE_Q4_0: a = 32; b = 18; break;
+    case QG_TYPE_Q4_K: a = 256; b = 144; break;
+    case QG_TYPE_Q6_K: a = 256; b = 210; break;
+    default: return QG_EUNSUPPORTED;
+  }
+  if (qk) *qk = a;
+  if (block_bytes) *block_bytes = b;
+  return QG_OK;
+}
+
+qg_status qg_device_status(uint32_t *status_out, int clear) {
+  if (!status_out) return QG_EINVAL_PTR;
+  if (cudaDeviceSynchronize() != cudaSuccess) return QG_ECUDA;
+  const unsigned int a = qg::read_status_gemv(clear != 0);
+  const unsigned int b = qg::read_status_moe(clear != 0);
+  const unsigned int c = qg::read_status_gemm(clear != 0);
+  if (a == 0xFFFFFFFFu || b == 0xFFFFFFFFu || c == 0xFFFFFFFFu) return QG_ECUDA;
+  *status_out = a | b | c;
+  return QG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,160 @@
+// qg_common.cuh -- shared device helpers for the sm_103a kernels: mbarrier and bulk-copy
+// (TMA) wrappers with bounded waits, the device status word, and exact in-register decode
+// helpers for the block formats.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ggufdq.h"
+
+#define QG_DEVICE __device__ __forceinline__
+
+// ---------------------------------------------------------------------------------------
+// Device status word (one per translation unit; qg_device_status ORs them).
+// ---------------------------------------------------------------------------------------
+#define QG_STATUS_BIT_ID (1u << QG_EDEVICE_ID)
+#define QG_STATUS_BIT_TIMEOUT (1u << QG_ETIMEOUT)
+
+// Polls of mbarrier.try_wait before a wait is declared expired.  Each poll may suspend the
+// thread for a hardware-defined interval, so this bounds every wait to well under a second
+// of a healthy GPU's time while never firing on a correct pipeline.
+#define QG_WAIT_LIMIT (1u << 22)
+
+// ---------------------------------------------------------------------------------------
+// Shared-memory addressing and mbarriers
+// ---------------------------------------------------------------------------------------
+QG_DEVICE uint32_t smem_u32(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+QG_DEVICE void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+QG_DEVICE void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+QG_DEVICE void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Arrive once and add `bytes` to the transaction count of the current phase.
+QG_DEVICE void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+QG_DEVICE void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+QG_DEVICE bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.  Returns false (and the
+// caller must abandon its work) when the limit expires.
+QG_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < QG_WAIT_LIMIT; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// ---------------------------------------------------------------------------------------
+// Bulk copies global -> shared (the TMA engine's non-tensor form).  Both addresses must be
+// 16-byte aligned and the size a multiple of 16; completion is signalled on `bar` as
+// transaction bytes.
+// ---------------------------------------------------------------------------------------
+QG_DEVICE void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst_smem)),
+      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// L2 prefetch of a global range (no completion tracking); size multiple of 16.
+QG_DEVICE void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
+// Named barrier among `nthreads` threads (multiple of 32) on barrier id `id` (1..15).
+QG_DEVICE void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------------------
+// Shared-memory loads used by the decoders: 32-bit shared-window addresses with the
+// offset folded into the instruction.  Not volatile, but ordered after the mbarrier
+// waits by their "memory" clobber dependency on the address-producing code.
+// ---------------------------------------------------------------------------------------
+#define QG_LDS32(addr, off, out) asm("ld.shared.b32 %0, [%1+" #off "];" : "=r"(out) : "r"(addr) : "memory")
+#define QG_LDS16(addr, off, out)                                                        \
+  do {                                                                                  \
+    uint16_t qg_t16_;                                                                   \
+    asm("ld.shared.b16 %0, [%1+" #off "];" : "=h"(qg_t16_) : "r"(addr) : "memory");     \
+    (out) = qg_t16_;                                                                    \
+  } while (0)
+#define QG_LDS128(addr, off, o0, o1, o2, o3) \
+  asm("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4+" #off "];" : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3) : "r"(addr) : "memory")
+#define QG_LDSF4(addr, off, v)                                                                  \
+  asm("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4+" #off "];" : "=f"((v).x), "=f"((v).y), "=f"((v).z), \
+      "=f"((v).w)                                                                               \
+      : "r"(addr)                                                                               \
+      : "memory")
+
+QG_DEVICE uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  QG_LDS32(addr, 0, v);
+  return v;
+}
+QG_DEVICE uint32_t lds_u16(uint32_t addr) {
+  uint32_t v;
+  QG_LDS16(addr, 0, v);
+  return v;
+}
+QG_DEVICE uint4 lds_v4(uint32_t addr) {
+  uint4 v;
+  QG_LDS128(addr, 0, v.x, v.y, v.z, v.w);
+  return v;
+}
+QG_DEVICE float4 lds_f4(uint32_t addr) {
+  float4 v;
+  QG_LDSF4(addr, 0, v);
+  return v;
+}
+
+// ---------------------------------------------------------------------------------------
+// Exact small-integer -> f32 conversion.  A byte u placed in the low mantissa bits of the
+// float 2^23 (bit pattern 0x4B0000uu) is the float 2^23 + u exactly; subtracting 2^23 + c
+// gives u - c exactly.  This uses the integer byte-permute unit instead of the slower
+// integer-to-float conversion path.
+// ---------------------------------------------------------------------------------------
+QG_DEVICE float magic_byte(uint32_t word, uint32_t byte_idx) {
+  // result bytes (LSB first): word[byte_idx], 0x00, 0x00, 0x4B
+  return __uint_as_float(__byte_perm(word, 0x4B000000u, 0x7440u | byte_idx));
+}
+
+// Packed f32x2 arithmetic (sm_100+): two IEEE f32 operations per instruction, through the
+// toolkit's float2 intrinsics so that operands live in register pairs.
+using f2 = float2;
+QG_DEVICE f2 mk2(float a, float b) { return make_float2(a, b); }
+QG_DEVICE f2 add2(f2 a, f2 b) { return __fadd2_rn(a, b); }
+QG_DEVICE f2 mul2(f2 a, f2 b) { return __fmul2_rn(a, b); }
+QG_DEVICE f2 fma2(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
+
+// f16 bits -> f32 (exact; hardware conversion).
+QG_DEVICE float h2f(uint32_t bits16) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
+}
+
+QG_DEVICE float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}

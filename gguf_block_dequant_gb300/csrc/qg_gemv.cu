@@ -1,0 +1,555 @@
+// qg_gemv.cu -- dense quantized GEMV over 1..16 token columns on sm_103a.
+//
+// Y[t][m] = sum_k W[m][k] * X[t][k] with W in raw GGUF blocks (matmulQ8 / matmulQ4 /
+// matmulQ6K for one token, matmulQ8T for a token batch, in the engine pages of the
+// diskformer package), f32 activations and f32 accumulation.
+//
+// Design (persistent CTAs, one per SM; every warp runs its own pipeline):
+//   - each warp owns row blocks of 4 rows and NS shared-memory slots with one mbarrier
+//     each.  Lane 0 issues the warp's next stages ahead with 1-D bulk copies (the TMA
+//     engine, cp.async.bulk): a stage is the warp's 4 rows times one K chunk, one copy per
+//     row segment (or one copy for 4 whole rows, which are contiguous in the raw layout).
+//     No producer warp: on this GPU a single issuing thread caps a CTA's bulk-copy rate well
+//     below HBM speed, while per-warp issue streams at full bandwidth.
+//   - the warp decodes its rows straight from the raw blocks in shared memory
+//     (qg_decode.cuh), reusing every activation load for its 4 rows, and keeps the
+//     accumulators in registers across the row's chunks.
+//   - activations: when all T rows fit in shared memory they are loaded once (2-D tensor
+//     copies with the 128-byte swizzle); otherwise they come in double-buffered K chunks
+//     that every warp walks in step, Y accumulating across chunks.
+//   - with few rows, KW warps split a row block's chunks and meet at a named barrier to sum
+//     their partials in a fixed order (deterministic).
+//   - every weight byte crosses HBM once per call, whatever T is.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "qg_decode.cuh"
+#include "qg_host.h"
+
+__device__ unsigned int g_qg_status_gemv;
+
+namespace {
+
+constexpr int kMaxNS = 4;  // slots per warp
+
+struct GemvArgs {
+  const uint8_t *w;
+  float *y;
+  long long row_bytes;
+  long long total_bytes;
+  int M, N, T;
+  int mode;          // 0: activations resident; 1: activations in K chunks (one per weight chunk)
+  int KC;            // elements per weight chunk (multiple of SG)
+  int nchunks;       // chunks per row
+  int xR;            // activation rows (32 floats) per token in one buffer
+  int rblocks;       // row blocks of 4 rows
+  int max_kw;        // most warps that may split one row block (mode 0; <= nchunks)
+  int NS;            // slots per warp
+  int stage_bytes;   // bytes per slot
+  int seg_slot;      // bytes per row segment inside a slot; 0: 4 whole rows in one copy
+  int box_rows;      // rows per activation tensor copy
+  uint32_t off_x, off_ring, off_red;
+  uint32_t xbuf_bytes;
+};
+
+QG_DEVICE void set_status(unsigned int bits) { atomicOr(&g_qg_status_gemv, bits); }
+
+QG_DEVICE void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// T activation rows blocks [row0(t), row0(t) + xR) into the buffer at dst (1024-byte aligned),
+// with expect_tx on bar
+QG_DEVICE void load_x(uint8_t *dst, const CUtensorMap *map, int T, int N, int c, int xR, int box_rows,
+                      uint64_t *bar) {
+  mbar_arrive_expect_tx(bar, static_cast<uint32_t>(T * xR) * 128u);
+  for (int t = 0; t < T; ++t)
+    for (int b = 0; b < xR; b += box_rows) tma_load_2d(dst + (t * xR + b) * 128, map, 0, t * (N / 32) + c * xR + b, bar);
+}
+
+// Bytes to bulk-copy for [src, src + n) where src may be unaligned: the copy starts at the
+// 16-byte boundary below src (dst receives src at dst + (src & 15)); bytes past the
+// tensor's last 16-byte boundary `mend` are written here with plain loads instead.
+QG_DEVICE uint32_t stage_copy(uint8_t *dst, uintptr_t src, uint32_t n, uintptr_t mend, uint64_t *, bool) {
+  const uintptr_t al = src & ~static_cast<uintptr_t>(15);
+  const uintptr_t want = (src + n + 15) & ~static_cast<uintptr_t>(15);
+  if (want <= mend) return static_cast<uint32_t>(want - al);  // the usual case
+  const uint32_t nb = mend > al ? static_cast<uint32_t>(mend - al) : 0u;
+  for (uintptr_t p = al + nb; p < src + n; ++p) dst[p - al] = *reinterpret_cast<const uint8_t *>(p);
+  return nb;
+}
+
+// Item cursor of one warp: tile index q (within the CTA) and chunk c.
+struct Cursor {
+  int q, c;
+};
+
+template <int QT, int TT, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant__ CUtensorMap xmap, const GemvArgs a) {
+  using D = Dec<QT>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t *wbar = reinterpret_cast<uint64_t *>(smem);  // [NW][kMaxNS]
+  uint64_t *xfull = wbar + NW * kMaxNS;                  // [2]
+  float *red = reinterpret_cast<float *>(smem + a.off_red);  // [2][NW][4][TT]
+  uint8_t *xs = smem + a.off_x;
+  uint8_t *ring = smem + a.off_ring;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = static_cast<int>(gridDim.x);
+  // this CTA's contiguous, balanced range of row blocks
+  const long long rbA = static_cast<long long>(blockIdx.x) * a.rblocks / G;
+  const long long rbB = static_cast<long long>(blockIdx.x + 1) * a.rblocks / G;
+  const int nrb = static_cast<int>(rbB - rbA);
+  // warps per row block: 1 when the CTA has at least NW row blocks, else the CTA's warps
+  // split each row block's chunks (mode 0 only)
+  int KW = 1;
+  if (a.mode == 0 && nrb < NW) KW = max(1, min(NW / max(nrb, 1), a.max_kw));
+  const int kw = warp % KW, rbl = warp / KW;
+  const int nslots = NW / KW;                       // row-block lanes in this CTA
+  const bool active = rbl < nslots && (nrb >= NW || rbl < nrb);
+  const int my_rbs = active ? (nrb - rbl + nslots - 1) / nslots : 0;  // row blocks rbA + rbl + i * nslots
+  const int xbytes_token = a.xR * 128;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NW * kMaxNS; ++i) mbar_init(&wbar[i], 1);
+    mbar_init(&xfull[0], 1);
+    mbar_init(&xfull[1], 1);
+    fence_mbar_init();
+    load_x(xs, &xmap, a.T, a.N, 0, a.xR, a.box_rows, &xfull[0]);
+    if (a.mode == 1 && a.nchunks > 1) load_x(xs + a.xbuf_bytes, &xmap, a.T, a.N, 1, a.xR, a.box_rows, &xfull[1]);
+  }
+  __syncthreads();
+
+  // ---- this warp's item sequence: (i-th row block of this warp, chunk c)
+  auto first = [&]() { return Cursor{0, a.mode == 0 ? kw : 0}; };
+  auto next = [&](Cursor u) {
+    if (a.mode == 0) {
+      u.c += KW;
+      if (u.c >= a.nchunks) {
+        u.c = kw;
+        ++u.q;
+      }
+    } else if (++u.q >= my_rbs) {
+      u.q = 0;
+      ++u.c;
+    }
+    return u;
+  };
+  // mode 1 walks every chunk (with my_rbs == 0 the warp only joins the chunk barriers)
+  auto valid = [&](Cursor u) { return a.mode == 0 ? u.q < my_rbs : u.c < a.nchunks; };
+  auto rb_of = [&](Cursor u) { return rbA + rbl + static_cast<long long>(u.q) * nslots; };
+
+  const uintptr_t wbase = reinterpret_cast<uintptr_t>(a.w);
+  const uintptr_t mend = (wbase + static_cast<uintptr_t>(a.total_bytes)) & ~static_cast<uintptr_t>(15);
+  const long long chunk_bytes = static_cast<long long>(a.KC / D::QK) * D::BB;
+  uint8_t *wring = ring + warp * a.NS * a.stage_bytes;
+  const uint32_t wring_s = smem_u32(wring);
+
+  // Issue the stage of item u into slot s.  Lane r copies row r's segment (lane 0 copies 4
+  // whole rows at once); the byte count goes to the slot's mbarrier before any copy starts.
+  const bool pad_rows = a.seg_slot != 0;
+  auto issue = [&](Cursor u, int s) {
+    const long long rb = rb_of(u);
+    const int nr = (my_rbs == 0) ? 0 : static_cast<int>(max(0LL, min(4LL, a.M - rb * 4)));
+    uint8_t *st = wring + s * a.stage_bytes;
+    uint64_t *bar = &wbar[warp * kMaxNS + s];
+    uintptr_t src = 0;
+    uint32_t n = 0;
+    uint8_t *dst = st;
+    if (!pad_rows) {
+      if (lane == 0) {
+        src = wbase + static_cast<uintptr_t>(rb * 4 * a.row_bytes);
+        n = static_cast<uint32_t>(nr * a.row_bytes);
+      }
+    } else if (lane < nr) {
+      const int kel = min(a.N - u.c * a.KC, a.KC);
+      n = static_cast<uint32_t>(kel / D::QK) * D::BB;
+      src = wbase + static_cast<uintptr_t>((rb * 4 + lane) * a.row_bytes + u.c * chunk_bytes);
+      dst = st + lane * a.seg_slot;
+    }
+    uint32_t nb = 0;
+    if (n) nb = stage_copy(dst, src, n, mend, bar, false);  // size, and tail bytes past mend
+    const uint32_t tx = __reduce_add_sync(0xFFFFFFFFu, nb);
+    if (lane == 0) mbar_arrive_expect_tx(bar, tx);
+    __syncwarp();
+    if (nb) {
+      fence_proxy_async_smem();  // the slot's previous bytes were read through the generic proxy
+      bulk_g2s(dst, reinterpret_cast<const void *>(src & ~static_cast<uintptr_t>(15)), nb, bar);
+    }
+  };
+
+  // prologue: the first NS - 1 items
+  Cursor ic = first();
+  int is = 0, issued = 0;
+  for (int i = 0; i < a.NS - 1 && valid(ic); ++i) {
+    issue(ic, is);
+    ic = next(ic);
+    is = (is + 1 == a.NS) ? 0 : is + 1;
+    ++issued;
+  }
+
+  const uint32_t wo = static_cast<uint32_t>(D::woff(lane));
+  uint32_t xo[D::NCH];
+#pragma unroll
+  for (int ch = 0; ch < D::NCH; ++ch) xo[ch] = x_lane_off<QT>(lane, ch);
+  const int gpc = a.KC / D::SG;
+
+  bool ok = true;
+  if (!mbar_wait(&xfull[0], 0)) ok = false;
+  float acc1[4];
+  f2 acc2[4][TT];
+  Cursor cc = first();
+  int cs = 0, cround = 0, consumed = 0;
+  int cur_xc = 0;  // activation chunk the warp is on (mode 1)
+  while (valid(cc)) {
+    // keep NS - 1 stages in flight ahead of this one
+    if (valid(ic)) {
+      issue(ic, is);
+      ic = next(ic);
+      is = (is + 1 == a.NS) ? 0 : is + 1;
+      ++issued;
+    }
+    if (a.mode == 1 && cc.c != cur_xc) {  // every warp is done with chunk cur_xc
+      named_bar_sync(1, NW * 32);
+      if (threadIdx.x == 0 && cur_xc + 2 < a.nchunks)
+        load_x(xs + (cur_xc & 1) * a.xbuf_bytes, &xmap, a.T, a.N, cur_xc + 2, a.xR, a.box_rows, &xfull[cur_xc & 1]);
+      cur_xc = cc.c;
+      if (ok && !mbar_wait(&xfull[cur_xc & 1], (cur_xc >> 1) & 1)) ok = false;
+    }
+    const long long rb = rb_of(cc);
+    const bool first_chunk = (a.mode == 1) || (cc.c == kw);
+    const bool last_chunk = (a.mode == 1) || (cc.c + KW >= a.nchunks);
+    if (first_chunk) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        acc1[r] = 0.f;
+#pragma unroll
+        for (int t = 0; t < TT; ++t) acc2[r][t] = mk2(0.f, 0.f);
+      }
+    }
+    if (ok && !mbar_wait(&wbar[warp * kMaxNS + cs], cround & 1)) ok = false;
+    if (ok) {
+      const int kel = min(a.N - cc.c * a.KC, a.KC);
+      const int gcount = (kel + D::SG - 1) / D::SG;
+      const uint32_t st = wring_s + static_cast<uint32_t>(cs * a.stage_bytes);
+      uint32_t wrow[4];
+      {
+        // low 32 bits suffice: only the address modulo 16 matters
+        const uint32_t r0 = static_cast<uint32_t>(wbase) + static_cast<uint32_t>(rb * 4) * static_cast<uint32_t>(a.row_bytes);
+        const uint32_t cb = static_cast<uint32_t>(cc.c) * static_cast<uint32_t>(chunk_bytes);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          if (!pad_rows)
+            wrow[r] = st + (r0 & 15u) + static_cast<uint32_t>(r) * static_cast<uint32_t>(a.row_bytes) + wo;
+          else
+            wrow[r] = st + static_cast<uint32_t>(r * a.seg_slot) +
+                      ((r0 + static_cast<uint32_t>(r) * static_cast<uint32_t>(a.row_bytes) + cb) & 15u) + wo;
+        }
+      }
+      // activation base of this chunk's first group
+      const uint32_t xg0 = smem_u32(xs) + (a.mode == 0 ? static_cast<uint32_t>(cc.c * gpc * (D::SG * 4))
+                                                        : static_cast<uint32_t>(cc.c & 1) * a.xbuf_bytes);
+      for (int g = 0; g < gcount; ++g) {
+        if (g * D::SG + D::block_first(lane) >= kel) break;
+        const uint32_t goff = static_cast<uint32_t>(g * D::GB);
+        const uint32_t xg = xg0 + static_cast<uint32_t>(g * (D::SG * 4));
+        if constexpr (TT == 1) {
+          float4 xc[D::NCH];
+#pragma unroll
+          for (int ch = 0; ch < D::NCH; ++ch) xc[ch] = lds_f4(xg + xo[ch]);
+          const float aux = D::xaux(xc);
+          typename D::U u[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) u[r] = D::load(wrow[r] + goff, lane);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc1[r] += D::dot1(u[r], xc, aux);
+        } else {
+          typename D::U u[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) u[r] = D::load(wrow[r] + goff, lane);
+#pragma unroll
+          for (int ch = 0; ch < D::NCH; ++ch) {
+            f2 w01[4], w23[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) D::weights(u[r], ch, w01[r], w23[r]);
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+              if (t < a.T) {
+                const float4 xv = lds_f4(xg + static_cast<uint32_t>(t * xbytes_token) + xo[ch]);
+                const f2 x01 = mk2(xv.x, xv.y), x23 = mk2(xv.z, xv.w);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                  acc2[r][t] = fma2(w01[r], x01, acc2[r][t]);
+                  acc2[r][t] = fma2(w23[r], x23, acc2[r][t]);
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();  // every lane is done reading this slot before lane 0 refills it
+    ++consumed;
+    if (++cs == a.NS) {
+      cs = 0;
+      ++cround;
+    }
+
+    if (last_chunk && my_rbs > 0) {
+      const bool accum = (a.mode == 1 && cc.c > 0);
+      if (KW == 1) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+#pragma unroll
+          for (int t = 0; t < TT; ++t) {
+            if (t < a.T) {
+              const float v = warp_sum(TT == 1 ? acc1[r] : acc2[r][t].x + acc2[r][t].y);
+              const long long row = rb * 4 + r;
+              if (lane == 0 && ok && row < a.M) {
+                float *p = a.y + static_cast<long long>(t) * a.M + row;
+                *p = accum ? *p + v : v;
+              }
+            }
+          }
+        }
+      } else {
+        float *myred = red + (((cc.q & 1) * NW + warp) * 4) * TT;  // double-buffered by row block
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+#pragma unroll
+          for (int t = 0; t < TT; ++t) {
+            if (t < a.T) {
+              const float v = warp_sum(TT == 1 ? acc1[r] : acc2[r][t].x + acc2[r][t].y);
+              if (lane == 0) myred[r * TT + t] = v;
+            }
+          }
+        }
+        named_bar_sync(2 + rbl, KW * 32);
+        if (kw == 0) {
+          const float *base = red + (((cc.q & 1) * NW + rbl * KW) * 4) * TT;
+          for (int idx = lane; idx < 4 * a.T; idx += 32) {
+            const int r = idx / a.T, t = idx - r * a.T;
+            float sum = 0.f;
+            for (int k = 0; k < KW; ++k) sum += base[(k * 4 + r) * TT + t];
+            const long long row = rb * 4 + r;
+            if (ok && row < a.M) a.y[static_cast<long long>(t) * a.M + row] = sum;
+          }
+        }
+      }
+    }
+    cc = next(cc);
+  }
+  if (!ok) {
+    if (lane == 0) set_status(QG_STATUS_BIT_TIMEOUT);
+    // never leave this warp's copies in flight
+    if (lane == 0)
+      for (int i = consumed; i < issued; ++i) mbar_wait(&wbar[warp * kMaxNS + (i % a.NS)], (i / a.NS) & 1);
+  }
+  if (threadIdx.x == 0 && a.mode == 1) {
+    // the last activation chunks were waited by every warp; nothing else is in flight
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Host side
+// ------------------------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+template <int QT, int TT>
+qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N, int T, cudaStream_t stream) {
+  using D = Dec<QT>;
+  constexpr int NW = (TT == 1) ? 16 : 8;
+  const qg::DeviceInfo &dev = qg::device_info();
+  if (!dev.ok) return QG_ECUDA;
+  const int ngroups = static_cast<int>((N + D::SG - 1) / D::SG);
+  const long long row_bytes = N / D::QK * D::BB;
+  const long long budget = dev.smem_optin - 4096;
+  const uint32_t hdr = 1024;
+  const uint32_t red_bytes = 2 * NW * 4 * TT * 4;
+  const long long xres = ((static_cast<long long>(T) * ngroups * D::SG * 4 + 1023) / 1024) * 1024;
+
+  GemvArgs a{};
+  int mode = (xres <= 100 * 1024) ? 0 : 1;
+  int gpc = 0, NS = 0, seg_slot = 0;
+  long long stage = 0;
+  uint32_t xbuf = 0;
+  auto plan_ring = [&](long long ring_avail) {
+    // stages of ~4-6 KB: 4 whole rows when they fit, else 4 row segments of gpc groups
+    const long long target = std::max<long long>(2048, std::min<long long>(6144, ring_avail / (3LL * NW)));
+    const long long whole = ((4 * row_bytes + 15) & ~15LL) + 32;
+    if (mode == 0 && whole <= target) {
+      gpc = ngroups;
+      seg_slot = 0;
+      stage = whole;
+    } else {
+      gpc = static_cast<int>(std::max<long long>(1, target / (4LL * D::GB)));
+      gpc = std::min(gpc, ngroups);
+      seg_slot = static_cast<int>(((static_cast<long long>(gpc) * D::GB + 15) & ~15LL) + 32);
+      stage = 4LL * seg_slot;
+    }
+    NS = static_cast<int>(std::min<long long>(kMaxNS, ring_avail / (static_cast<long long>(NW) * stage)));
+  };
+  if (mode == 0) {
+    xbuf = static_cast<uint32_t>(xres);
+    plan_ring(budget - hdr - red_bytes - xbuf - 1024);
+    if (NS < 2) mode = 1;
+  }
+  if (mode == 1) {
+    // activation chunks double-buffered: each chunk is gpc groups of every token
+    const long long per_group = static_cast<long long>(T) * D::SG * 4;
+    int g = static_cast<int>(std::max<long long>(1, (40 * 1024) / per_group));
+    g = std::min(g, ngroups);
+    while (true) {
+      xbuf = static_cast<uint32_t>(((per_group * g + 1023) / 1024) * 1024);
+      const long long ring_avail = budget - hdr - red_bytes - 2LL * xbuf - 1024;
+      gpc = g;
+      seg_slot = static_cast<int>(((static_cast<long long>(gpc) * D::GB + 15) & ~15LL) + 32);
+      stage = 4LL * seg_slot;
+      NS = ring_avail > 0 ? static_cast<int>(std::min<long long>(kMaxNS, ring_avail / (static_cast<long long>(NW) * stage)))
+                          : 0;
+      if (NS >= 3 || g == 1) break;
+      g = std::max(1, g / 2);
+    }
+    if (NS < 2) return QG_EUNSUPPORTED;
+  }
+  int nchunks = (ngroups + gpc - 1) / gpc;
+  const long long rblocks = (M + 3) / 4;
+  // when a CTA gets fewer row blocks than warps its warps split K: make sure there are
+  // enough chunks for that (stages then shrink to a group or two)
+  const long long rb_per_cta = (rblocks + dev.sms - 1) / dev.sms;
+  if (mode == 0 && rb_per_cta < NW) {
+    const int want_kw = static_cast<int>(std::min<long long>(NW, NW / std::max<long long>(1, rb_per_cta)));
+    while (gpc > 1 && (ngroups + gpc - 1) / gpc < want_kw) {
+      gpc = std::max(1, gpc / 2);
+      seg_slot = static_cast<int>(((static_cast<long long>(gpc) * D::GB + 15) & ~15LL) + 32);
+      stage = 4LL * seg_slot;
+    }
+    nchunks = (ngroups + gpc - 1) / gpc;
+  }
+  a.w = static_cast<const uint8_t *>(w);
+  a.y = y;
+  a.row_bytes = row_bytes;
+  a.total_bytes = row_bytes * M;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.T = T;
+  a.mode = mode;
+  a.KC = gpc * D::SG;
+  a.nchunks = nchunks;
+  a.xR = (mode == 0 ? ngroups * D::SG : a.KC) / 32;
+  a.rblocks = static_cast<int>(rblocks);
+  a.max_kw = nchunks;
+  a.NS = NS;
+  a.stage_bytes = static_cast<int>(stage);
+  a.seg_slot = seg_slot;
+  a.xbuf_bytes = xbuf;
+  int box = 8;
+  for (int d = 8; d <= 256; d += 8)
+    if (a.xR % d == 0) box = d;
+  a.box_rows = box;
+  a.off_red = hdr;
+  a.off_x = (hdr + red_bytes + 1023) & ~1023u;
+  a.off_ring = a.off_x + (mode == 0 ? 1u : 2u) * xbuf;
+  const uint32_t smem = a.off_ring + static_cast<uint32_t>(NW * NS * stage) + 1024 + 64;
+
+  // activation tensor map: [T*N/32 rows][32 f32], 128-byte swizzle, box [box][32]
+  auto enc = encode_fn();
+  if (!enc) return QG_ECUDA;
+  CUtensorMap map;
+  const cuuint64_t gdim[2] = {32, static_cast<cuuint64_t>(T) * static_cast<cuuint64_t>(N / 32)};
+  const cuuint64_t gstride[1] = {128};
+  const cuuint32_t boxd[2] = {32, static_cast<cuuint32_t>(box)};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(x), gdim, gstride, boxd, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return QG_ECUDA;
+
+  auto kern = qgemv_kernel<QT, TT, NW>;
+  if (!qg::set_smem_attr(reinterpret_cast<const void *>(kern), smem)) return QG_ECUDA;
+  const int grid = static_cast<int>(std::min<long long>(rblocks, dev.sms));
+  kern<<<grid, NW * 32, smem, stream>>>(map, a);
+  return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+}
+
+template <int QT>
+qg_status launch_type(const void *w, const float *x, float *y, int64_t M, int64_t N, int T, cudaStream_t s) {
+  if (T == 1) return launch_t<QT, 1>(w, x, y, M, N, T, s);
+  if (T <= 2) return launch_t<QT, 2>(w, x, y, M, N, T, s);
+  if (T <= 4) return launch_t<QT, 4>(w, x, y, M, N, T, s);
+  if (T <= 8) return launch_t<QT, 8>(w, x, y, M, N, T, s);
+  return launch_t<QT, 16>(w, x, y, M, N, T, s);
+}
+
+}  // namespace
+
+namespace qg {
+
+qg_status gemv_dispatch(int type, const void *w, const float *x, float *y, int64_t M, int64_t N, int T,
+                        cudaStream_t s) {
+  int qk = 0, bb = 0;
+  if (qg_block_shape(type, &qk, &bb) != QG_OK) return QG_EUNSUPPORTED;
+  if (!w || !x || !y) return QG_EINVAL_PTR;
+  if (M < 0 || N <= 0 || N % qk || T < 1 || T > 16 || M > INT32_MAX || N > INT32_MAX) return QG_EINVAL_SHAPE;
+  if (static_cast<long long>(T) * N > INT32_MAX) return QG_EINVAL_SHAPE;
+  if (!aligned16(w) || !aligned16(x) || !aligned16(y)) return QG_EALIGN;
+  if (M == 0) return QG_OK;
+  switch (type) {
+    case QG_TYPE_Q8_0: return launch_type<QG_TYPE_Q8_0>(w, x, y, M, N, T, s);
+    case QG_TYPE_Q4_0: return launch_type<QG_TYPE_Q4_0>(w, x, y, M, N, T, s);
+    case QG_TYPE_Q4_K: return launch_type<QG_TYPE_Q4_K>(w, x, y, M, N, T, s);
+    case QG_TYPE_Q6_K: return launch_type<QG_TYPE_Q6_K>(w, x, y, M, N, T, s);
+    default: return QG_EUNSUPPORTED;
+  }
+}
+
+unsigned int read_status_gemv(bool clear) {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_qg_status_gemv, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  if (clear) {
+    const unsigned int z = 0;
+    cudaMemcpyToSymbol(g_qg_status_gemv, &z, sizeof(z));
+  }
+  return v;
+}
+
+}  // namespace qg
+
+extern "C" {
+
+qg_status qgemv_q8_0(const void *w, const float *x, float *y, int64_t M, int64_t N, qg_stream_t s) {
+  return qg::gemv_dispatch(QG_TYPE_Q8_0, w, x, y, M, N, 1, reinterpret_cast<cudaStream_t>(s));
+}
+qg_status qgemv_q4_0(const void *w, const float *x, float *y, int64_t M, int64_t N, qg_stream_t s) {
+  return qg::gemv_dispatch(QG_TYPE_Q4_0, w, x, y, M, N, 1, reinterpret_cast<cudaStream_t>(s));
+}
+qg_status qgemv_q4_k(const void *w, const float *x, float *y, int64_t M, int64_t N, qg_stream_t s) {
+  return qg::gemv_dispatch(QG_TYPE_Q4_K, w, x, y, M, N, 1, reinterpret_cast<cudaStream_t>(s));
+}
+qg_status qgemv_q6_k(const void *w, const float *x, float *y, int64_t M, int64_t N, qg_stream_t s) {
+  return qg::gemv_dispatch(QG_TYPE_Q6_K, w, x, y, M, N, 1, reinterpret_cast<cudaStream_t>(s));
+}
+qg_status qgemv_t(int type, const void *w, const float *x, float *y, int64_t M, int64_t N, int T, qg_stream_t s) {
+  return qg::gemv_dispatch(type, w, x, y, M, N, T, reinterpret_cast<cudaStream_t>(s));
+}
+
+}  // extern "C"

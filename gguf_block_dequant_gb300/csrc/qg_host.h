@@ -1,0 +1,34 @@
+// qg_host.h -- host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ggufdq.h"
+
+namespace qg {
+
+struct DeviceInfo {
+  bool ok = false;
+  int sms = 0;         // streaming multiprocessors
+  int smem_optin = 0;  // max dynamic shared memory per block (opt-in)
+  int l2_bytes = 0;
+};
+
+// Properties of the current device (queried once per device).
+const DeviceInfo &device_info();
+
+// Raise a kernel's dynamic shared-memory limit on the current device (cached).
+bool set_smem_attr(const void *func, uint32_t bytes);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// dense GEMV entry shared by qgemv_* / qgemv_t / qgemm (small T) / MoE helpers
+qg_status gemv_dispatch(int type, const void *w, const float *x, float *y, int64_t M, int64_t N, int T,
+                        cudaStream_t s);
+
+unsigned int read_status_gemv(bool clear);
+unsigned int read_status_moe(bool clear);
+unsigned int read_status_gemm(bool clear);
+
+}  // namespace qg

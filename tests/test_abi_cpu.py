@@ -1,0 +1,58 @@
+"""The C ABI on the CPU: the library builds, loads without a GPU, exports every symbol the
+header declares, and rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ggufdq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gguf_block_dequant_gb300 import build
+
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def _declared():
+    src = open(HEADER).read()
+    return re.findall(r"^QG_API [^;(]*?\b([a-z_0-9]+)\(", src, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 15, names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in ggufdq.h but not exported"
+
+
+def test_version_strings_and_block_shapes(lib):
+    assert lib.qg_version() == 1
+    lib.qg_strerror.restype = ctypes.c_char_p
+    assert lib.qg_strerror(0) == b"ok"
+    assert lib.qg_strerror(999) == b"unknown status"
+    qk, bb = ctypes.c_int(), ctypes.c_int()
+    for t, (q, b) in {8: (32, 34), 2: (32, 18), 12: (256, 144), 14: (256, 210)}.items():
+        assert lib.qg_block_shape(t, ctypes.byref(qk), ctypes.byref(bb)) == 0
+        assert (qk.value, bb.value) == (q, b)
+    assert lib.qg_block_shape(1, ctypes.byref(qk), ctypes.byref(bb)) == 4  # QG_EUNSUPPORTED
+
+
+def test_host_argument_checks_need_no_gpu(lib):
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    lib.qgemv_q8_0.argtypes = [P, P, P, I64, I64, P]
+    lib.qgemv_t.argtypes = [ctypes.c_int, P, P, P, I64, I64, ctypes.c_int, P]
+    # NULL pointers -> QG_EINVAL_PTR, before any CUDA call
+    assert lib.qgemv_q8_0(None, None, None, 4, 64, None) == 2
+    fake = P(4096)  # never dereferenced: the shape check fails first
+    assert lib.qgemv_q8_0(fake, fake, fake, 4, 48, None) == 1      # N % 32 != 0
+    assert lib.qgemv_q8_0(fake, fake, fake, -1, 64, None) == 1     # M < 0
+    assert lib.qgemv_t(8, fake, fake, fake, 4, 64, 0, None) == 1   # T < 1
+    assert lib.qgemv_t(8, fake, fake, fake, 4, 64, 17, None) == 1  # T > 16
+    assert lib.qgemv_t(13, fake, fake, fake, 4, 64, 1, None) == 4  # unsupported type
+    odd = P(4096 + 2)
+    assert lib.qgemv_q8_0(odd, fake, fake, 4, 64, None) == 3       # misaligned weights

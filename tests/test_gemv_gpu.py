@@ -1,0 +1,163 @@
+"""Parity of the dense quantized GEMV kernels (qgemv_*, qgemv_t) with the CPU oracle.
+
+Every call goes through the C ABI (libggufdq.so) via the thin Python binding.  Sizes span
+several tiles, partial activation groups and ragged row tails; the one-hot cases check that
+every dequantized weight comes out of the kernels bit-exact.
+"""
+import numpy as np
+import pytest
+
+import gguf_synth as gs
+from helpers import assert_within_bound, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TYPES = [gs.Q8_0, gs.Q4_0, gs.Q4_K, gs.Q6_K]
+
+
+@pytest.fixture(scope="module")
+def qg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gguf_block_dequant_gb300 as qg
+    from gguf_block_dequant_gb300 import build
+
+    build.build()
+    qg.load()
+    return qg
+
+
+def _run(qg, qtype, w, x, M, N):
+    T = x.shape[0]
+    wd = to_dev(w, torch)
+    xd = to_dev(x, torch)
+    yd = torch.full((T, M), float("nan"), dtype=torch.float32, device="cuda")
+    if T == 1:
+        qg.qgemv(qtype, wd, xd, M, N, yd)
+    else:
+        qg.qgemv_t(qtype, wd, xd, yd, M, N, T)
+    torch.cuda.synchronize()
+    assert qg.device_status() == 0
+    return yd.cpu().numpy()
+
+
+def _shapes(qtype):
+    qk = gs.BLOCK[qtype][0]
+    if qk == 32:   # groups of 256 elements: full groups, a partial group, a single block
+        return [(1, 32), (37, 352), (130, 1024), (261, 2816), (9, 4096 + 96)]
+    return [(1, 256), (37, 1280), (130, 2048), (67, 5120), (5, 17408)]
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8, 11, 16])
+def test_gemv_parity(qg, oracle_lib, qtype, T):
+    for si, (M, N) in enumerate(_shapes(qtype)):
+        w = gs.quant_blocks(qtype, M, N, seed=si, stream=qtype)
+        x = gs.activations(T, N, seed=si, stream=7)
+        y = _run(qg, qtype, w, x, M, N)
+        ref, bnd = oracle_lib.gemv(qtype, w, M, N, x, threads=4)
+        assert_within_bound(y, ref, bnd, what=f"type {qtype} M={M} N={N} T={T}")
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+def test_gemv_one_hot_is_exact_dequant(qg, oracle_lib, qtype):
+    """x = e_k makes every product but one an exact zero, so y must equal column k of the
+    dequantized matrix bit for bit: this checks the in-register decode of every type."""
+    M, N = 45, 2048 if gs.BLOCK[qtype][0] == 256 else 640
+    w = gs.quant_blocks(qtype, M, N, seed=3, stream=qtype)
+    W = oracle_lib.dequant(qtype, w, M, N)
+    cols = list(range(0, N, 7)) + [N - 1]
+    for T in (1, 8):
+        for start in range(0, len(cols), T):
+            ks = cols[start:start + T]
+            x = np.zeros((len(ks), N), np.float32)
+            for t, k in enumerate(ks):
+                x[t, k] = 1.0
+            y = _run(qg, qtype, w, x, M, N)
+            for t, k in enumerate(ks):
+                # equal as values: exact for every nonzero weight; a zero weight may come out
+                # as +0 where the decoded value is -0 (negative Q6_K scales)
+                assert np.array_equal(y[t], W[:, k]), (qtype, T, k)
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+def test_gemv_zero_input_and_zero_rows(qg, qtype):
+    M, N = 70, 1024
+    w = gs.quant_blocks(qtype, M, N, seed=4, stream=qtype)
+    y = _run(qg, qtype, w, np.zeros((3, N), np.float32), M, N)
+    assert (y == 0).all()
+
+
+def test_gemv_chunked_activations(qg, oracle_lib):
+    """T = 16 over a long row streams the activations in K chunks (y accumulated per chunk)."""
+    for qtype, (M, N) in [(gs.Q8_0, (40, 9728)), (gs.Q4_K, (24, 17408)), (gs.Q6_K, (24, 17408)),
+                          (gs.Q4_0, (40, 9728))]:
+        w = gs.quant_blocks(qtype, M, N, seed=5, stream=qtype)
+        x = gs.activations(16, N, seed=5)
+        y = _run(qg, qtype, w, x, M, N)
+        ref, bnd = oracle_lib.gemv(qtype, w, M, N, x, threads=4)
+        assert_within_bound(y, ref, bnd, what=f"chunked type {qtype}")
+
+
+def test_gemv_rejects_bad_arguments(qg):
+    w = torch.zeros(34 * 4, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(128, dtype=torch.float32, device="cuda")
+    y = torch.zeros(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(qg.QGError) as e:
+        qg.qgemv(gs.Q8_0, w, x, 1, 100, y)      # N not a multiple of 32
+    assert e.value.status == qg.QG_EINVAL_SHAPE
+    with pytest.raises(qg.QGError) as e:
+        qg.qgemv(gs.Q8_0, w[1:], x, 1, 128, y)  # misaligned weights
+    assert e.value.status == qg.QG_EALIGN
+    with pytest.raises(qg.QGError) as e:
+        qg.qgemv_t(gs.Q8_0, w, x, y, 1, 128, 17)
+    assert e.value.status == qg.QG_EINVAL_SHAPE
+    with pytest.raises(qg.QGError) as e:
+        qg.qgemv_t(5, w, x, y, 1, 128, 1)
+    assert e.value.status == qg.QG_EUNSUPPORTED
+
+
+# ---- full-size workloads (sampled rows) ------------------------------------------------------
+
+def _sample_rows(M, n=96, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[0, 1, M // 2, M - 2, M - 1], rng.integers(0, M, n)]))
+    return rows
+
+
+@pytest.mark.parametrize("name", list(gs.QWEN3_4B_PROJ))
+@pytest.mark.parametrize("T", [1, 4, 16])
+def test_qwen3_4b_projection_full_size(qg, oracle_lib, name, T):
+    M, N = gs.QWEN3_4B_PROJ[name]
+    w = gs.quant_blocks(gs.Q8_0, M, N, seed=0, stream=100 + list(gs.QWEN3_4B_PROJ).index(name))
+    x = gs.activations(T, N, seed=0)
+    y = _run(qg, gs.Q8_0, w, x, M, N)
+    rows = _sample_rows(M)
+    rb = gs.row_bytes(gs.Q8_0, N)
+    wsub = w.reshape(M, rb)[rows]
+    ref, bnd = oracle_lib.gemv(gs.Q8_0, wsub, len(rows), N, x, threads=4)
+    assert_within_bound(y[:, rows], ref, bnd, what=f"{name} T={T}")
+
+
+@pytest.mark.parametrize("qtype,M,N", [(gs.Q4_K, 17408, 5120), (gs.Q4_K, 5120, 17408), (gs.Q6_K, 17408, 5120),
+                                        (gs.Q6_K, 5120, 17408), (gs.Q4_0, 2112, 2816)])
+@pytest.mark.parametrize("T", [1, 8])
+def test_kquant_full_size(qg, oracle_lib, qtype, M, N, T):
+    w = gs.quant_blocks(qtype, M, N, seed=0, stream=200 + qtype)
+    x = gs.activations(T, N, seed=0)
+    y = _run(qg, qtype, w, x, M, N)
+    rows = _sample_rows(M)
+    rb = gs.row_bytes(qtype, N)
+    ref, bnd = oracle_lib.gemv(qtype, w.reshape(M, rb)[rows], len(rows), N, x, threads=4)
+    assert_within_bound(y[:, rows], ref, bnd, what=f"type {qtype} {M}x{N} T={T}")
+
+
+def test_config1_full(qg, oracle_lib):
+    """Q8_0 1024 x 1024, T = 1, seed 0: every row against the oracle."""
+    M = N = 1024
+    w = gs.quant_blocks(gs.Q8_0, M, N, seed=0)
+    x = gs.activations(1, N, seed=0)
+    y = _run(qg, gs.Q8_0, w, x, M, N)
+    ref, bnd = oracle_lib.gemv(gs.Q8_0, w, M, N, x, threads=4)
+    assert_within_bound(y, ref, bnd, what="config 1")
