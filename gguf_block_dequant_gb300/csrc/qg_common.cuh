@@ -158,3 +158,45 @@ QG_DEVICE float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
   return v;
 }
+
+// Butterfly reduce-scatter of N per-lane partial values (N a power of two, N <= 64): at each
+// step a lane keeps half of its values and adds the partner's copy of that half, so the
+// warp needs N - 1 + (5 - log2 N) shuffles instead of 5 N.  Afterwards v[0] holds the full
+// sum of value rs_index(lane) (N <= 32; lanes that differ only in their low 5 - log2 N bits
+// hold the same value), or v[0], v[1] hold values 2 lane and 2 lane + 1 (N = 64).
+template <int N>
+QG_DEVICE void reduce_scatter(float (&v)[N], int lane) {
+  static_assert(N >= 1 && N <= 64 && (N & (N - 1)) == 0, "power of two up to 64");
+#pragma unroll
+  for (int s = 0; s < 5; ++s) {
+    const int o = 16 >> s;
+    const int m = N >> s;  // values held before this step
+    if (m >= 2) {
+      const bool hi = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < (N + 1) / 2; ++i) {
+        if (i < m / 2) {
+          const float send = hi ? v[i] : v[i + m / 2];
+          const float keep = hi ? v[i + m / 2] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+        }
+      }
+    } else {
+      v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], o);
+    }
+  }
+}
+
+template <int N>
+QG_DEVICE constexpr int rs_shift() {
+  return N >= 32 ? 0 : N >= 16 ? 1 : N >= 8 ? 2 : N >= 4 ? 3 : N >= 2 ? 4 : 5;
+}
+// value index held in v[0] by this lane, and whether this lane is the one that owns it
+template <int N>
+QG_DEVICE int rs_index(int lane) {
+  return N == 64 ? 2 * lane : (lane >> rs_shift<N>());
+}
+template <int N>
+QG_DEVICE bool rs_owner(int lane) {
+  return (lane & ((1 << rs_shift<N>()) - 1)) == 0;
+}

@@ -23,10 +23,9 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <mutex>
-
 #include "qg_decode.cuh"
 #include "qg_host.h"
+#include "qg_pipe.cuh"
 
 __device__ unsigned int g_qg_status_gemv;
 
@@ -50,40 +49,12 @@ struct GemvArgs {
   int stage_bytes;   // bytes per slot
   int seg_slot;      // bytes per row segment inside a slot; 0: 4 whole rows in one copy
   int box_rows;      // rows per activation tensor copy
-  uint32_t off_x, off_ring, off_red;
+  int maxq;          // most row blocks of one warp (mode 1 partial sums)
+  uint32_t off_x, off_ring, off_red, off_part;
   uint32_t xbuf_bytes;
 };
 
 QG_DEVICE void set_status(unsigned int bits) { atomicOr(&g_qg_status_gemv, bits); }
-
-QG_DEVICE void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// T activation rows blocks [row0(t), row0(t) + xR) into the buffer at dst (1024-byte aligned),
-// with expect_tx on bar
-QG_DEVICE void load_x(uint8_t *dst, const CUtensorMap *map, int T, int N, int c, int xR, int box_rows,
-                      uint64_t *bar) {
-  mbar_arrive_expect_tx(bar, static_cast<uint32_t>(T * xR) * 128u);
-  for (int t = 0; t < T; ++t)
-    for (int b = 0; b < xR; b += box_rows) tma_load_2d(dst + (t * xR + b) * 128, map, 0, t * (N / 32) + c * xR + b, bar);
-}
-
-// Bytes to bulk-copy for [src, src + n) where src may be unaligned: the copy starts at the
-// 16-byte boundary below src (dst receives src at dst + (src & 15)); bytes past the
-// tensor's last 16-byte boundary `mend` are written here with plain loads instead.
-QG_DEVICE uint32_t stage_copy(uint8_t *dst, uintptr_t src, uint32_t n, uintptr_t mend, uint64_t *, bool) {
-  const uintptr_t al = src & ~static_cast<uintptr_t>(15);
-  const uintptr_t want = (src + n + 15) & ~static_cast<uintptr_t>(15);
-  if (want <= mend) return static_cast<uint32_t>(want - al);  // the usual case
-  const uint32_t nb = mend > al ? static_cast<uint32_t>(mend - al) : 0u;
-  for (uintptr_t p = al + nb; p < src + n; ++p) dst[p - al] = *reinterpret_cast<const uint8_t *>(p);
-  return nb;
-}
 
 // Item cursor of one warp: tile index q (within the CTA) and chunk c.
 struct Cursor {
@@ -97,7 +68,8 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *wbar = reinterpret_cast<uint64_t *>(smem);  // [NW][kMaxNS]
   uint64_t *xfull = wbar + NW * kMaxNS;                  // [2]
-  float *red = reinterpret_cast<float *>(smem + a.off_red);  // [2][NW][4][TT]
+  float *red = reinterpret_cast<float *>(smem + a.off_red);    // [2][NW][4][TT]
+  float *part = reinterpret_cast<float *>(smem + a.off_part);  // [NW][maxq][4][TT] (mode 1)
   uint8_t *xs = smem + a.off_x;
   uint8_t *ring = smem + a.off_ring;
 
@@ -303,43 +275,49 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
     }
 
     if (last_chunk && my_rbs > 0) {
-      const bool accum = (a.mode == 1 && cc.c > 0);
+      // the 4 x TT row sums, reduce-scattered over the warp (each lane ends up owning one or
+      // two of them)
+      constexpr int NV = 4 * TT;
+      constexpr int NH = NV == 64 ? 2 : 1;
+      float v[NV];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int t = 0; t < TT; ++t) v[r * TT + t] = (TT == 1) ? acc1[r] : acc2[r][t].x + acc2[r][t].y;
+      reduce_scatter<NV>(v, lane);
+      const int i0 = rs_index<NV>(lane);
+      const bool own = rs_owner<NV>(lane);
       if (KW == 1) {
+        // mode 1: partial sums of the row block's K chunks stay in shared memory, added in
+        // chunk order; y is written once, after the last chunk
+        float *pacc = part + (warp * a.maxq + cc.q) * NV;
+        const bool final_chunk = (a.mode == 0) || (cc.c + 1 == a.nchunks);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-#pragma unroll
-          for (int t = 0; t < TT; ++t) {
-            if (t < a.T) {
-              const float v = warp_sum(TT == 1 ? acc1[r] : acc2[r][t].x + acc2[r][t].y);
-              const long long row = rb * 4 + r;
-              if (lane == 0 && ok && row < a.M) {
-                float *p = a.y + static_cast<long long>(t) * a.M + row;
-                *p = accum ? *p + v : v;
-              }
-            }
+        for (int h = 0; h < NH; ++h) {
+          const int idx = i0 + h;
+          const int r = idx / TT, t = idx - r * TT;
+          float val = v[h];
+          if (own && a.mode == 1) {
+            if (cc.c > 0) val += pacc[idx];
+            if (!final_chunk) pacc[idx] = val;
           }
+          const long long row = rb * 4 + r;
+          if (own && final_chunk && ok && t < a.T && row < a.M) a.y[static_cast<long long>(t) * a.M + row] = val;
         }
       } else {
-        float *myred = red + (((cc.q & 1) * NW + warp) * 4) * TT;  // double-buffered by row block
+        float *myred = red + ((cc.q & 1) * NW + warp) * NV;  // double-buffered by row block
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-#pragma unroll
-          for (int t = 0; t < TT; ++t) {
-            if (t < a.T) {
-              const float v = warp_sum(TT == 1 ? acc1[r] : acc2[r][t].x + acc2[r][t].y);
-              if (lane == 0) myred[r * TT + t] = v;
-            }
-          }
-        }
+        for (int h = 0; h < NH; ++h)
+          if (own) myred[i0 + h] = v[h];
         named_bar_sync(2 + rbl, KW * 32);
         if (kw == 0) {
-          const float *base = red + (((cc.q & 1) * NW + rbl * KW) * 4) * TT;
-          for (int idx = lane; idx < 4 * a.T; idx += 32) {
-            const int r = idx / a.T, t = idx - r * a.T;
+          const float *base = red + ((cc.q & 1) * NW + rbl * KW) * NV;
+          for (int idx = lane; idx < NV; idx += 32) {
+            const int r = idx / TT, t = idx - r * TT;
             float sum = 0.f;
-            for (int k = 0; k < KW; ++k) sum += base[(k * 4 + r) * TT + t];
+            for (int k = 0; k < KW; ++k) sum += base[k * NV + idx];
             const long long row = rb * 4 + r;
-            if (ok && row < a.M) a.y[static_cast<long long>(t) * a.M + row] = sum;
+            if (ok && t < a.T && row < a.M) a.y[static_cast<long long>(t) * a.M + row] = sum;
           }
         }
       }
@@ -352,27 +330,11 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
     if (lane == 0)
       for (int i = consumed; i < issued; ++i) mbar_wait(&wbar[warp * kMaxNS + (i % a.NS)], (i / a.NS) & 1);
   }
-  if (threadIdx.x == 0 && a.mode == 1) {
-    // the last activation chunks were waited by every warp; nothing else is in flight
-  }
 }
 
 // ------------------------------------------------------------------------------------------
 // Host side
 // ------------------------------------------------------------------------------------------
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
 
 template <int QT, int TT>
 qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N, int T, cudaStream_t stream) {
@@ -388,9 +350,12 @@ qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N
   const long long xres = ((static_cast<long long>(T) * ngroups * D::SG * 4 + 1023) / 1024) * 1024;
 
   GemvArgs a{};
-  int mode = (xres <= 100 * 1024) ? 0 : 1;
+  const long long rblocks = (M + 3) / 4;
+  const long long rb_per_cta = (rblocks + dev.sms - 1) / dev.sms;
+  // activations resident (mode 0) when that still leaves the warps a ring of >= 48 KB
+  int mode = (xres + 48 * 1024 <= budget - hdr - red_bytes - 1024) ? 0 : 1;
   int gpc = 0, NS = 0, seg_slot = 0;
-  long long stage = 0;
+  long long stage = 0, part_bytes = 0;
   uint32_t xbuf = 0;
   auto plan_ring = [&](long long ring_avail) {
     // stages of ~4-6 KB: 4 whole rows when they fit, else 4 row segments of gpc groups
@@ -418,9 +383,11 @@ qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N
     const long long per_group = static_cast<long long>(T) * D::SG * 4;
     int g = static_cast<int>(std::max<long long>(1, (40 * 1024) / per_group));
     g = std::min(g, ngroups);
+    // per-warp partial sums of its row blocks across chunks
+    part_bytes = ((static_cast<long long>(NW) * ((rb_per_cta + NW - 1) / NW) * 4 * TT * 4) + 1023) & ~1023LL;
     while (true) {
       xbuf = static_cast<uint32_t>(((per_group * g + 1023) / 1024) * 1024);
-      const long long ring_avail = budget - hdr - red_bytes - 2LL * xbuf - 1024;
+      const long long ring_avail = budget - hdr - red_bytes - 2LL * xbuf - part_bytes - 1024;
       gpc = g;
       seg_slot = static_cast<int>(((static_cast<long long>(gpc) * D::GB + 15) & ~15LL) + 32);
       stage = 4LL * seg_slot;
@@ -432,10 +399,8 @@ qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N
     if (NS < 2) return QG_EUNSUPPORTED;
   }
   int nchunks = (ngroups + gpc - 1) / gpc;
-  const long long rblocks = (M + 3) / 4;
   // when a CTA gets fewer row blocks than warps its warps split K: make sure there are
   // enough chunks for that (stages then shrink to a group or two)
-  const long long rb_per_cta = (rblocks + dev.sms - 1) / dev.sms;
   if (mode == 0 && rb_per_cta < NW) {
     const int want_kw = static_cast<int>(std::min<long long>(NW, NW / std::max<long long>(1, rb_per_cta)));
     while (gpc > 1 && (ngroups + gpc - 1) / gpc < want_kw) {
@@ -468,11 +433,13 @@ qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N
   a.box_rows = box;
   a.off_red = hdr;
   a.off_x = (hdr + red_bytes + 1023) & ~1023u;
-  a.off_ring = a.off_x + (mode == 0 ? 1u : 2u) * xbuf;
+  a.maxq = static_cast<int>((rb_per_cta + NW - 1) / NW);
+  a.off_part = a.off_x + (mode == 0 ? 1u : 2u) * xbuf;
+  a.off_ring = a.off_part + static_cast<uint32_t>(part_bytes);
   const uint32_t smem = a.off_ring + static_cast<uint32_t>(NW * NS * stage) + 1024 + 64;
 
   // activation tensor map: [T*N/32 rows][32 f32], 128-byte swizzle, box [box][32]
-  auto enc = encode_fn();
+  auto enc = qg::encode_fn();
   if (!enc) return QG_ECUDA;
   CUtensorMap map;
   const cuuint64_t gdim[2] = {32, static_cast<cuuint64_t>(T) * static_cast<cuuint64_t>(N / 32)};

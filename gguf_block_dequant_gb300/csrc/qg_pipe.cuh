@@ -1,0 +1,105 @@
+// qg_pipe.cuh -- pieces of the warp-autonomous streaming pipeline shared by the GEMV and
+// MoE kernels: activation tensor copies, unaligned bulk-copy sizing, the one-token row-block
+// inner loop, and the host-side tensor-map encoder.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "qg_decode.cuh"
+
+QG_DEVICE void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// T activation rows blocks [row0(t), row0(t) + xR) into the buffer at dst (1024-byte aligned),
+// with expect_tx on bar
+QG_DEVICE void load_x(uint8_t *dst, const CUtensorMap *map, int T, int N, int c, int xR, int box_rows,
+                      uint64_t *bar) {
+  mbar_arrive_expect_tx(bar, static_cast<uint32_t>(T * xR) * 128u);
+  for (int t = 0; t < T; ++t)
+    for (int b = 0; b < xR; b += box_rows) tma_load_2d(dst + (t * xR + b) * 128, map, 0, t * (N / 32) + c * xR + b, bar);
+}
+
+// Bytes to bulk-copy for [src, src + n) where src may be unaligned: the copy starts at the
+// 16-byte boundary below src (dst receives src at dst + (src & 15)); bytes past the
+// tensor's last 16-byte boundary `mend` are written here with plain loads instead.
+QG_DEVICE uint32_t stage_copy(uint8_t *dst, uintptr_t src, uint32_t n, uintptr_t mend, uint64_t *, bool) {
+  const uintptr_t al = src & ~static_cast<uintptr_t>(15);
+  const uintptr_t want = (src + n + 15) & ~static_cast<uintptr_t>(15);
+  if (want <= mend) return static_cast<uint32_t>(want - al);  // the usual case
+  const uint32_t nb = mend > al ? static_cast<uint32_t>(mend - al) : 0u;
+  for (uintptr_t p = al + nb; p < src + n; ++p) dst[p - al] = *reinterpret_cast<const uint8_t *>(p);
+  return nb;
+}
+
+
+// One-token inner loop over the groups of a stage: 4 rows (shared-memory unit addresses
+// wrow[r], already offset by the lane's unit) against the activation chunk whose first
+// group starts at shared address xg0; xo[ch] are the lane's swizzled chunk offsets.
+// Accumulates into acc[4].  kel is the number of valid elements in this chunk.
+template <int QT>
+QG_DEVICE void rows_dot1(const uint32_t (&wrow)[4], uint32_t xg0, const uint32_t (&xo)[Dec<QT>::NCH], int kel, int lane,
+                         float (&acc)[4]) {
+  using D = Dec<QT>;
+  const int gcount = (kel + D::SG - 1) / D::SG;
+  for (int g = 0; g < gcount; ++g) {
+    if (g * D::SG + D::block_first(lane) >= kel) break;
+    const uint32_t goff = static_cast<uint32_t>(g * D::GB);
+    const uint32_t xg = xg0 + static_cast<uint32_t>(g * (D::SG * 4));
+    float4 xc[D::NCH];
+#pragma unroll
+    for (int ch = 0; ch < D::NCH; ++ch) xc[ch] = lds_f4(xg + xo[ch]);
+    const float aux = D::xaux(xc);
+    typename D::U u[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) u[r] = D::load(wrow[r] + goff, lane);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[r] += D::dot1(u[r], xc, aux);
+  }
+}
+
+namespace qg {
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+
+// Tensor map over a token-major f32 [rows][K] activation matrix viewed as [rows * K / 32]
+// rows of 32 floats, 128-byte swizzle, boxes of box_rows rows.  K % 32 == 0.
+inline bool encode_x_map(CUtensorMap *map, const float *x, long long rows, long long K, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t gdim[2] = {32, static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(K / 32)};
+  const cuuint64_t gstride[1] = {128};
+  const cuuint32_t boxd[2] = {32, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(x), gdim, gstride, boxd, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Largest box height (multiple of 8, <= 256) dividing rows.
+inline int box_rows_for(int rows) {
+  int box = 8;
+  for (int d = 8; d <= 256; d += 8)
+    if (rows % d == 0) box = d;
+  return box;
+}
+
+}  // namespace qg

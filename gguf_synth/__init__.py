@@ -48,13 +48,15 @@ class Stream:
 
     def __init__(self, seed: int, stream: int):
         key = np.array([seed & 0xFFFFFFFFFFFFFFFF, stream & 0xFFFFFFFFFFFFFFFF], dtype=np.uint64)
-        self._bg = np.random.Philox(key=key)
+        # full-range uint64 draws return the generator's raw words unchanged (the same
+        # sequence as Philox.random_raw), through numpy's faster bulk fill
+        self._gen = np.random.Generator(np.random.Philox(key=key))
 
     def words(self, n: int) -> np.ndarray:
         out = np.empty(n, dtype=np.uint64)
         for s in range(0, n, _CHUNK):
             e = min(n, s + _CHUNK)
-            out[s:e] = self._bg.random_raw(e - s)
+            out[s:e] = self._gen.integers(0, 1 << 64, size=e - s, dtype=np.uint64, endpoint=False)
         return out
 
     def bytes(self, n: int) -> np.ndarray:
@@ -72,14 +74,24 @@ class Stream:
         u2 = self.uniform01(n)
         return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
 
-    def ints(self, n: int, lo: int, hi: int) -> np.ndarray:
-        """Integers uniform in [lo, hi] (hi - lo < 65536) by 16-bit multiply-shift."""
+    def ints(self, n: int, lo: int, hi: int, dtype=np.int32) -> np.ndarray:
+        """Integers uniform in [lo, hi] (hi - lo < 65536) by 16-bit multiply-shift: value i
+        comes from the i-th 16-bit piece of the word stream (4 pieces per word, low first)."""
         span = hi - lo + 1
         if not 0 < span <= 65536:
             raise ValueError("span out of range")
-        w = self.words((n + 3) // 4)
-        u16 = w.view(np.uint16)[:n].astype(np.uint32)
-        return ((u16 * np.uint32(span)) >> np.uint32(16)).astype(np.int32) + lo
+        out = np.empty(n, dtype=dtype)
+        step = 4 * _CHUNK  # a multiple of 4 values: chunking never splits a word
+        for s in range(0, n, step):
+            e = min(n, s + step)
+            w = self.words((e - s + 3) // 4)
+            u = w.view(np.uint16)[:e - s].astype(np.uint32)
+            u *= np.uint32(span)
+            u >>= np.uint32(16)
+            v = u.view(np.int32)
+            v += lo
+            out[s:e] = v
+        return out
 
 
 def _f16_bytes(v: np.ndarray) -> np.ndarray:
@@ -112,7 +124,7 @@ def quant_blocks(qtype: int, rows: int, n: int, seed: int = 0, stream: int = 0) 
     g = lambda f: Stream(seed, _sub(stream, f))  # noqa: E731
     if qtype == Q8_0:
         out[:, 0:2] = _f16_bytes(np.abs(g(_S_D).normal(nblk)) * 0.02)
-        out[:, 2:34] = g(_S_Q).ints(nblk * 32, -127, 127).astype(np.int8).view(np.uint8).reshape(nblk, 32)
+        out[:, 2:34] = g(_S_Q).ints(nblk * 32, -127, 127, np.int8).view(np.uint8).reshape(nblk, 32)
     elif qtype == Q4_0:
         out[:, 0:2] = _f16_bytes(np.abs(g(_S_D).normal(nblk)) * 0.02)
         out[:, 2:18] = g(_S_Q).bytes(nblk * 16).reshape(nblk, 16)
@@ -124,7 +136,7 @@ def quant_blocks(qtype: int, rows: int, n: int, seed: int = 0, stream: int = 0) 
     elif qtype == Q6_K:
         out[:, 0:128] = g(_S_Q).bytes(nblk * 128).reshape(nblk, 128)
         out[:, 128:192] = g(_S_QH).bytes(nblk * 64).reshape(nblk, 64)
-        out[:, 192:208] = g(_S_SC).ints(nblk * 16, -32, 31).astype(np.int8).view(np.uint8).reshape(nblk, 16)
+        out[:, 192:208] = g(_S_SC).ints(nblk * 16, -32, 31, np.int8).view(np.uint8).reshape(nblk, 16)
         out[:, 208:210] = _f16_bytes(np.abs(g(_S_D).normal(nblk)) * 0.01)
     else:
         raise ValueError(f"unsupported type {qtype}")

@@ -56,3 +56,30 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.qgemv_t(13, fake, fake, fake, 4, 64, 1, None) == 4  # unsupported type
     odd = P(4096 + 2)
     assert lib.qgemv_q8_0(odd, fake, fake, 4, 64, None) == 3       # misaligned weights
+
+
+def test_moe_host_checks_need_no_gpu(lib):
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.moe_workspace_size.argtypes = [I, I, I, I, I]
+    lib.moe_workspace_size.restype = SZ
+    lib.moe_route_topk.argtypes = [P, P, I, I, I, I, P, P, P, P, SZ, P]
+    lib.moe_expert_swiglu.argtypes = [I, P, P, I64, P, I, I, P, P, I, I, I, I, P, P, SZ, P]
+    lib.moe_combine.argtypes = [I, P, I64, P, I, I, P, P, P, I, I, I, I, P, I, P, SZ, P]
+    # workspace: logits + tickets + dn + counters, each rounded to 256 bytes
+    n = lib.moe_workspace_size(8, 8, 128, 2048, 768)
+    assert n == 4096 + 256 + 8 * 8 * 2048 * 4 + 8 * 512 * 4
+    assert lib.moe_workspace_size(8, 33, 128, 2048, 768) == 0   # k > 32
+    assert lib.moe_workspace_size(8, 8, 300, 2048, 768) == 0    # E > 256
+    fake = P(4096)
+    assert lib.moe_route_topk(None, fake, 1, 64, 8, 2, fake, fake, None, fake, 1 << 20, None) == 2
+    assert lib.moe_route_topk(fake, fake, 1, 64, 8, 9, fake, fake, None, fake, 1 << 20, None) == 1  # k > E
+    assert lib.moe_route_topk(fake, fake, 1, 66, 8, 2, fake, fake, None, fake, 1 << 20, None) == 1  # H % 4
+    assert lib.moe_route_topk(fake, fake, 2, 64, 8, 2, fake, fake, None, fake, 16, None) == 8       # workspace
+    assert lib.moe_expert_swiglu(8, fake, fake, 0, None, 1, 8, fake, fake, 17, 2, 64, 32, fake, None, 0,
+                                 None) == 4  # more than 16 tokens: not on this path
+    assert lib.moe_expert_swiglu(8, fake, fake, 0, None, 1, 8, fake, fake, 2, 2, 48, 32, fake, None, 0,
+                                 None) == 1  # H not a multiple of the block
+    assert lib.moe_expert_swiglu(3, fake, fake, 0, None, 1, 8, fake, fake, 2, 2, 64, 32, fake, None, 0,
+                                 None) == 4  # unsupported type
+    assert lib.moe_combine(8, fake, 0, None, 1, 8, fake, fake, fake, 2, 2, 64, 32, fake, 1, fake, 16,
+                           None) == 8  # workspace too small
