@@ -84,6 +84,13 @@ QG_DEVICE void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes) {
 }
 
 // Named barrier among `nthreads` threads (multiple of 32) on barrier id `id` (1..15).
+// 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned); completes at
+// cp_async_wait_all()
+QG_DEVICE void cp_async16(uint32_t dst_smem, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+QG_DEVICE void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 QG_DEVICE void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -3,8 +3,8 @@
 // sequence on the engine pages: matmulF32 -> topk -> expertQ8 (gate||up) -> siluMulMoe ->
 // expertQ8 with inputPerSlot (down) -> moeAccum).
 //
-// Router: one warp per expert row of the f32 router matrix, all tokens of a 16-token tile
-// reused against each weight load; the last CTA of a token tile (ticket counter) takes the k
+// Router: one CTA per expert row of the f32 router matrix (its warps split the row), all
+// tokens of a 16-token tile reused against each weight load; the last CTA of a token tile (ticket counter) takes the k
 // greedy picks per token (one warp per token) and their renormalised softmax weights.
 //
 // Expert kernels (persistent, one CTA per SM): every CTA first groups the (token, pick)
@@ -36,7 +36,7 @@ namespace {
 
 constexpr int kMaxNS = 4;
 constexpr int kRouterTB = 16;  // tokens per router CTA
-constexpr int kRouterEPB = 4;  // experts (one per warp) per router CTA
+constexpr int kRouterWarps = 4;  // warps per router CTA (one expert per CTA)
 constexpr int kMaxE = 256;
 constexpr int kMaxK = 32;
 
@@ -96,44 +96,50 @@ QG_DEVICE void topk_token(const float *l, int E, int k, int lane, int32_t *ids, 
   }
 }
 
-__global__ void __launch_bounds__(kRouterEPB * 32) moe_router_kernel(const float *__restrict__ xn,
-                                                                      const float *__restrict__ wr, int T, int H,
-                                                                      int E, int k, float *logits, int32_t *ids,
-                                                                      float *weights, unsigned int *ticket) {
+// grid (E, token tiles of kRouterTB); kRouterWarps warps split the H dot of the CTA's expert
+__global__ void __launch_bounds__(kRouterWarps * 32) moe_router_kernel(const float *__restrict__ xn,
+                                                                        const float *__restrict__ wr, int T, int H,
+                                                                        int E, int k, float *logits, int32_t *ids,
+                                                                        float *weights, unsigned int *ticket) {
+  __shared__ float part[kRouterWarps][kRouterTB];
+  __shared__ unsigned int s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * kRouterEPB + warp;
+  const int e = blockIdx.x;
   const int t0 = blockIdx.y * kRouterTB;
   const int nt = min(kRouterTB, T - t0);
-  if (e < E) {
-    float acc[kRouterTB];
+  float acc[kRouterTB];
 #pragma unroll
-    for (int t = 0; t < kRouterTB; ++t) acc[t] = 0.f;
-    const float4 *w4 = reinterpret_cast<const float4 *>(wr + static_cast<size_t>(e) * H);
-    const float4 *x4 = reinterpret_cast<const float4 *>(xn + static_cast<size_t>(t0) * H);
-    const int H4 = H >> 2;
-    for (int h = lane; h < H4; h += 32) {
-      const float4 w = __ldg(w4 + h);
-#pragma unroll
-      for (int t = 0; t < kRouterTB; ++t) {
-        if (t < nt) {
-          const float4 x = __ldg(x4 + static_cast<size_t>(t) * H4 + h);
-          acc[t] = fmaf(w.x, x.x, acc[t]);
-          acc[t] = fmaf(w.y, x.y, acc[t]);
-          acc[t] = fmaf(w.z, x.z, acc[t]);
-          acc[t] = fmaf(w.w, x.w, acc[t]);
-        }
-      }
-    }
+  for (int t = 0; t < kRouterTB; ++t) acc[t] = 0.f;
+  const float4 *w4 = reinterpret_cast<const float4 *>(wr + static_cast<size_t>(e) * H);
+  const float4 *x4 = reinterpret_cast<const float4 *>(xn + static_cast<size_t>(t0) * H);
+  const int H4 = H >> 2;
+#pragma unroll 4
+  for (int h = warp * 32 + lane; h < H4; h += kRouterWarps * 32) {
+    const float4 w = __ldg(w4 + h);
 #pragma unroll
     for (int t = 0; t < kRouterTB; ++t) {
       if (t < nt) {
-        const float s = warp_sum(acc[t]);
-        if (lane == 0) logits[static_cast<size_t>(t0 + t) * E + e] = s;
+        const float4 x = __ldg(x4 + static_cast<size_t>(t) * H4 + h);
+        acc[t] = fmaf(w.x, x.x, acc[t]);
+        acc[t] = fmaf(w.y, x.y, acc[t]);
+        acc[t] = fmaf(w.z, x.z, acc[t]);
+        acc[t] = fmaf(w.w, x.w, acc[t]);
       }
     }
   }
+#pragma unroll
+  for (int t = 0; t < kRouterTB; ++t) {
+    const float s = warp_sum(acc[t]);
+    if (lane == 0) part[warp][t] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < nt) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRouterWarps; ++w) s += part[w][threadIdx.x];
+    logits[static_cast<size_t>(t0 + threadIdx.x) * E + e] = s;
+  }
   // the last CTA of this token tile to finish takes the picks
-  __shared__ unsigned int s_last;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -143,7 +149,7 @@ __global__ void __launch_bounds__(kRouterEPB * 32) moe_router_kernel(const float
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int t = t0 + warp; t < t0 + nt; t += kRouterEPB)
+  for (int t = t0 + warp; t < t0 + nt; t += kRouterWarps)
     topk_token(logits + static_cast<size_t>(t) * E, E, k, lane, ids + static_cast<size_t>(t) * k,
                weights + static_cast<size_t>(t) * k);
   __syncthreads();
@@ -311,13 +317,14 @@ QG_DEVICE int block_row(const MoeArgs &a, int p, int r) {
 QG_DEVICE float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
 // Token activation rows into shared memory in the 128-byte swizzled layout the decoders read
-// (16-byte unit j of 32-float row R at 128 R + 16 (j ^ (R & 7))).
-QG_DEVICE void store_x_row(uint8_t *xs, int slot, int xrow_bytes, const float *src, int K, int t0, int nthr) {
+// (16-byte unit j of 32-float row R at 128 R + 16 (j ^ (R & 7))), as asynchronous 16-byte
+// copies; the caller waits with cp_async_wait_all() and a CTA barrier.
+QG_DEVICE void copy_x_row(uint8_t *xs, int slot, int xrow_bytes, const float *src, int K, int t0, int nthr) {
   const int K4 = K >> 2;
+  const uint32_t base = smem_u32(xs) + static_cast<uint32_t>(slot * xrow_bytes);
   for (int i = t0; i < K4; i += nthr) {
-    const float4 v = __ldg(reinterpret_cast<const float4 *>(src) + i);
     const int R = i >> 3, j = i & 7;
-    *reinterpret_cast<float4 *>(xs + static_cast<size_t>(slot) * xrow_bytes + R * 128 + 16 * (j ^ (R & 7))) = v;
+    cp_async16(base + static_cast<uint32_t>(R * 128 + 16 * (j ^ (R & 7))), src + 4 * i);
   }
 }
 
@@ -362,15 +369,17 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
 
   // activations of the tokens this CTA needs
   if constexpr (!DOWN) {
-    for (int t = warp; t < a.T; t += NW)
-      store_x_row(xs, t, a.xrow_bytes, a.xin + static_cast<size_t>(t) * a.K, a.K, lane, 32);
+    for (int t = 0; t < a.T; ++t)
+      copy_x_row(xs, t, a.xrow_bytes, a.xin + static_cast<size_t>(t) * a.K, a.K, threadIdx.x, NW * 32);
   } else {
     for (int u = uA; u <= uB; ++u)
-      for (int t = warp; t < pl.u_cnt[u]; t += NW) {
+      for (int t = 0; t < pl.u_cnt[u]; ++t) {
         const int z = pl.s_pairs[pl.u_first[u] + t];
-        store_x_row(xs, (u - uA) * TT + t, a.xrow_bytes, a.xin + static_cast<size_t>(z) * a.K, a.K, lane, 32);
+        copy_x_row(xs, (u - uA) * TT + t, a.xrow_bytes, a.xin + static_cast<size_t>(z) * a.K, a.K, threadIdx.x,
+                   NW * 32);
       }
   }
+  cp_async_wait_all();
   __syncthreads();
 
   // ---- this warp's row blocks rbA + warp + i * NW, each in nchunks K chunks
@@ -645,9 +654,9 @@ qg_status route_impl(const float *xn, const float *wr, int T, int H, int E, int 
   if (ws_bytes < L.dn) return QG_EWORKSPACE;
   uint8_t *w = static_cast<uint8_t *>(ws);
   float *logits = logits_out ? logits_out : reinterpret_cast<float *>(w + L.logits);
-  const dim3 grid((E + kRouterEPB - 1) / kRouterEPB, (T + kRouterTB - 1) / kRouterTB);
+  const dim3 grid(E, (T + kRouterTB - 1) / kRouterTB);
   if (grid.y > 65535) return QG_EINVAL_SHAPE;
-  moe_router_kernel<<<grid, kRouterEPB * 32, 0, s>>>(xn, wr, T, H, E, k, logits, ids, weights,
+  moe_router_kernel<<<grid, kRouterWarps * 32, 0, s>>>(xn, wr, T, H, E, k, logits, ids, weights,
                                                      reinterpret_cast<unsigned int *>(w + L.ticket));
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
