@@ -16,7 +16,7 @@ resident in HBM; ``e2e`` is the same metric through the public binding with the 
 activations copied from pinned host memory and the head's logits copied back, every step.
 The step is captured once in a CUDA graph and replayed (253 launches per replay).
 With ``--sections all`` a ``detail`` object adds T = 4 / 16, per-projection times, the
-K-quant and Q4_0 shapes, and the MoE layer.  Multi-GPU: replicas only (each rank runs the
+K-quant and Q4_0 shapes, the MoE layer and the T = 512 prefill GEMM.  Multi-GPU: replicas only (each rank runs the
 same step on its own GPU; no data-path collective).
 """
 from __future__ import annotations
@@ -471,7 +471,45 @@ def run_detail(torch, qg, D, stream, args, hbm):
     out["q8_0_T1_per_projection"] = per
     out["kquant"] = run_kquant(torch, qg, stream, hbm)
     out["moe_layer"] = run_moe(torch, qg, stream, hbm)
+    out["prefill_gemm"] = run_gemm(torch, qg, stream)
     return out
+
+
+def run_gemm(torch, qg, stream):
+    """Prefill dequant-GEMM, Q8_0, T = 512: 9728x2560 and 2560x9728 (tcgen05, bf16 operands,
+    f32 accumulation), each call = X f32 -> bf16 conversion + the GEMM kernel, rotating over
+    weight copies that exceed 3x L2."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _, bf16_peak, src = peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    res = {}
+    T = 512
+    for M, N in ((9728, 2560), (2560, 9728)):
+        b = gs.tensor_bytes(gs.Q8_0, M, N)
+        R = max(2, -(-3 * l2 // b))
+        base = torch.from_numpy(gs.quant_blocks(gs.Q8_0, M, N, seed=0, stream=500)).to(dev)
+        ws_w = [base] + [base.clone() for _ in range(R - 1)]
+        x = torch.from_numpy(gs.activations(T, N, seed=0, stream=501)).to(dev)
+        y = torch.empty((T, M), dtype=torch.float32, device=dev)
+        ws = torch.empty(qg.qgemm_workspace_size(gs.Q8_0, M, N, T), dtype=torch.uint8, device=dev)
+
+        def calls():
+            for w in ws_w:
+                qg.qgemm(gs.Q8_0, w, x, y, M, N, T, ws)
+        g = capture(torch, calls, stream)
+        reps = 10
+        el = time_graph(torch, g, stream, reps, 3)
+        n = reps * R
+        us = el / n * 1e6
+        flop = 2.0 * M * N * T
+        tf = flop / (us * 1e-6) / 1e12
+        res[f"q8_0_{M}x{N}_T{T}"] = {"us": round(us, 2), "TFLOP/s": round(tf, 1),
+                                     "frac_bf16_peak": round(tf / bf16_peak, 4), "peak_source": src,
+                                     "weight_GB/s": round(b / (us * 1e-6) / 1e9, 1), "launches_per_call": 2}
+        del g
+    if qg.device_status() != 0:
+        raise RuntimeError("device status set in the GEMM benchmark")
+    return res
 
 
 def run_moe(torch, qg, stream, hbm, layers=8):

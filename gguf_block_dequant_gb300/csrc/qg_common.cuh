@@ -83,7 +83,6 @@ QG_DEVICE void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
 }
 
-// Named barrier among `nthreads` threads (multiple of 32) on barrier id `id` (1..15).
 // 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned); completes at
 // cp_async_wait_all()
 QG_DEVICE void cp_async16(uint32_t dst_smem, const void *src) {
@@ -91,6 +90,7 @@ QG_DEVICE void cp_async16(uint32_t dst_smem, const void *src) {
 }
 QG_DEVICE void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// Named barrier among `nthreads` threads (multiple of 32) on barrier id `id` (1..15).
 QG_DEVICE void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
