@@ -54,7 +54,9 @@ def parse():
     p.add_argument("--tokens", type=int, default=1, help="token columns T of the headline step (1..16)")
     p.add_argument("--layers", type=int, default=LAYERS)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--sections", choices=["main", "all"], default="all")
+    p.add_argument("--sections", choices=["main", "all", "gemm", "moe", "kquant", "proj"], default="all",
+                   help="main: the headline line only; all: plus the detail object; gemm / moe / kquant / "
+                        "proj: only that detail section, printed as its own JSON line (for profiling runs)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -312,6 +314,31 @@ def time_graph(torch, g, stream, steps, warmup):
     return e0.elapsed_time(e1) / 1e3
 
 
+def run_section(args):
+    """One detail section alone (no headline measurement), for short profiling runs."""
+    import torch
+
+    import gguf_block_dequant_gb300 as qg
+    from gguf_block_dequant_gb300 import build as qbuild
+
+    torch.cuda.set_device(0)
+    qbuild.build()
+    qg.load()
+    hbm, _, _ = peaks()
+    stream = torch.cuda.Stream()
+    if args.sections == "gemm":
+        res = run_gemm(torch, qg, stream, reps=args.steps, warmup=args.warmup)
+    elif args.sections == "moe":
+        res = run_moe(torch, qg, stream, hbm, reps=args.steps, warmup=args.warmup)
+    elif args.sections == "kquant":
+        res = run_kquant(torch, qg, stream, hbm, reps=args.steps, warmup=args.warmup)
+    else:
+        D = Decode(torch, qg, args.layers, args.tokens, torch.device("cuda", 0))
+        res = run_projections(torch, D, stream, hbm, reps=args.steps, warmup=args.warmup)
+    print(json.dumps({"section": args.sections, "result": res}), flush=True)
+    return 0
+
+
 def run_ours(args):
     import torch
 
@@ -455,27 +482,14 @@ def run_detail(torch, qg, D, stream, args, hbm):
                                     "us_per_step": round(el / steps * 1e6, 1),
                                     "tokens_per_s": round(T * steps / el, 1)}
         del g
-    # one projection at a time, rotating over the layer copies (T = 1)
-    per = {}
-    for name in PROJ + [HEAD]:
-        M, N = gs.QWEN3_4B_PROJ[name]
-        copies = D.w[name]
-        g = capture(torch, lambda name=name, copies=copies: [D.gemv(name, c, 1) for c in copies], stream)
-        reps = 20
-        el = time_graph(torch, g, stream, reps, 3)
-        n = reps * len(copies)
-        b = gs.tensor_bytes(gs.Q8_0, M, N)
-        per[name] = {"us": round(el / n * 1e6, 2), "GB/s": round(b * n / el / 1e9, 1),
-                     "frac_hbm": round(b * n / el / 1e9 / hbm, 4)}
-        del g
-    out["q8_0_T1_per_projection"] = per
+    out["q8_0_T1_per_projection"] = run_projections(torch, D, stream, hbm)
     out["kquant"] = run_kquant(torch, qg, stream, hbm)
     out["moe_layer"] = run_moe(torch, qg, stream, hbm)
     out["prefill_gemm"] = run_gemm(torch, qg, stream)
     return out
 
 
-def run_gemm(torch, qg, stream):
+def run_gemm(torch, qg, stream, reps=10, warmup=3):
     """Prefill dequant-GEMM, Q8_0, T = 512: 9728x2560 and 2560x9728 (tcgen05, bf16 operands,
     f32 accumulation), each call = X f32 -> bf16 conversion + the GEMM kernel, rotating over
     weight copies that exceed 3x L2."""
@@ -497,8 +511,7 @@ def run_gemm(torch, qg, stream):
             for w in ws_w:
                 qg.qgemm(gs.Q8_0, w, x, y, M, N, T, ws)
         g = capture(torch, calls, stream)
-        reps = 10
-        el = time_graph(torch, g, stream, reps, 3)
+        el = time_graph(torch, g, stream, reps, warmup)
         n = reps * R
         us = el / n * 1e6
         flop = 2.0 * M * N * T
@@ -512,7 +525,7 @@ def run_gemm(torch, qg, stream):
     return res
 
 
-def run_moe(torch, qg, stream, hbm, layers=8):
+def run_moe(torch, qg, stream, hbm, layers=8, reps=50, warmup=3):
     """Qwen3-30B-A3B-shaped MoE layer in Q8_0 (H 2048, F 768, 128 experts, top-8): one
     moe_layer call per layer, each layer with its own expert pool and its own input tokens,
     rotating over `layers` pools (8 x 641 MB, far above L2)."""
@@ -537,8 +550,7 @@ def run_moe(torch, qg, stream, hbm, layers=8):
                 qg.moe_layer(gs.Q8_0, xn[l], wr[l], p[go:], p[uo:], p[do:], stride, None, E, T, H, F, E, k,
                              ids[l], wts[l], act, x, ws)
         g = capture(torch, calls, stream)
-        reps = 50
-        el = time_graph(torch, g, stream, reps, 3)
+        el = time_graph(torch, g, stream, reps, warmup)
         n = reps * layers
         us = el / n * 1e6
         uniq = [len(np.unique(ids[l].cpu().numpy())) for l in range(layers)]
@@ -555,7 +567,23 @@ def run_moe(torch, qg, stream, hbm, layers=8):
     return res
 
 
-def run_kquant(torch, qg, stream, hbm):
+def run_projections(torch, D, stream, hbm, reps=20, warmup=3):
+    """One projection at a time (T = 1), rotating over its layer copies."""
+    per = {}
+    for name in PROJ + [HEAD]:
+        M, N = gs.QWEN3_4B_PROJ[name]
+        copies = D.w[name]
+        g = capture(torch, lambda name=name, copies=copies: [D.gemv(name, c, 1) for c in copies], stream)
+        el = time_graph(torch, g, stream, reps, warmup)
+        n = reps * len(copies)
+        b = gs.tensor_bytes(gs.Q8_0, M, N)
+        per[name] = {"us": round(el / n * 1e6, 2), "GB/s": round(b * n / el / 1e9, 1),
+                     "frac_hbm": round(b * n / el / 1e9 / hbm, 4)}
+        del g
+    return per
+
+
+def run_kquant(torch, qg, stream, hbm, reps=10, warmup=3):
     """Q4_K / Q6_K 17408x5120 and 5120x17408, Q4_0 2112x2816, Q8_0 1024x1024 at T in {1, 8},
     each rotating over enough weight copies to exceed 3x L2."""
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -578,8 +606,7 @@ def run_kquant(torch, qg, stream, hbm):
                     else:
                         qg.qgemv_t(qt, w, x, y, M, N, T)
             g = capture(torch, calls, stream)
-            reps = 10
-            el = time_graph(torch, g, stream, reps, 3)
+            el = time_graph(torch, g, stream, reps, warmup)
             n = reps * R
             key = f"{gs.TYPE_NAME[qt]}_{M}x{N}_T{T}"
             res[key] = {"us": round(el / n * 1e6, 2), "GB/s": round(b * n / el / 1e9, 1),
@@ -593,6 +620,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.sections not in ("main", "all"):
+        return run_section(args)
     return run_ours(args)
 
 

@@ -17,10 +17,13 @@
 #define QG_STATUS_BIT_ID (1u << QG_EDEVICE_ID)
 #define QG_STATUS_BIT_TIMEOUT (1u << QG_ETIMEOUT)
 
-// Polls of mbarrier.try_wait before a wait is declared expired.  Each poll may suspend the
-// thread for a hardware-defined interval, so this bounds every wait to well under a second
-// of a healthy GPU's time while never firing on a correct pipeline.
-#define QG_WAIT_LIMIT (1u << 22)
+// Time after which a wait on an mbarrier is declared expired (nanoseconds of the GPU's
+// global timer).  Far above any healthy pipeline's wait, far below a watchdog's patience.
+#define QG_WAIT_NS 200000000ull
+// Suspend-time hint of one mbarrier.try_wait (nanoseconds): a waiting thread sleeps until the
+// phase completes or this much time has passed, instead of spinning on the issue slots the
+// working warps need.
+#define QG_TRY_WAIT_HINT_NS 1000000u
 
 // ---------------------------------------------------------------------------------------
 // Shared-memory addressing and mbarriers
@@ -57,12 +60,35 @@ QG_DEVICE bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+QG_DEVICE uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// try_wait that lets the hardware suspend the thread (up to the hint) while the phase is
+// incomplete
+QG_DEVICE bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(QG_TRY_WAIT_HINT_NS)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false (and the
-// caller must abandon its work) when the limit expires.
+// caller must abandon its work) once QG_WAIT_NS has passed.
 QG_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  for (uint32_t i = 0; i < QG_WAIT_LIMIT; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (global_ns() - t0 > QG_WAIT_NS) return false;
+  }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -89,6 +115,19 @@ QG_DEVICE void cp_async16(uint32_t dst_smem, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
 }
 QG_DEVICE void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// one arrival on `bar` once every cp.async this thread issued before it has landed (the
+// barrier's expected count covers these arrivals)
+QG_DEVICE void cp_async_mbar_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Programmatic dependent launch: wait until the preceding kernel in the stream has completed
+// and its memory is visible (a no-op when the launch did not allow the overlap), and let the
+// next kernel start its prologue early.  Kernels call wait before touching any input or
+// output, and launch_dependents only after their wait, so every kernel that has started can
+// rely on all kernels two or more launches back having completed.
+QG_DEVICE void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+QG_DEVICE void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Named barrier among `nthreads` threads (multiple of 32) on barrier id `id` (1..15).
 QG_DEVICE void named_bar_sync(int id, int nthreads) {

@@ -14,7 +14,7 @@
 //   warp 1      TMEM allocation and the single MMA-issuing thread: per 64-k stage four
 //               tcgen05.mma.kind::f16 (M 128, N 256, K 16, bf16 x bf16 -> f32), then
 //               tcgen05.commit to the stage's "empty" barrier;
-//   warps 2-9   converters: decode the stage's 128 x 64 weights from the raw ring (d * q in
+//   warps 2-17  converters: decode the stage's 128 x 64 weights from the raw ring (d * q in
 //               f32, one rounding to bf16) into the A slot in the UMMA K-major 128-byte
 //               swizzled layout; after a tile's last stage they are the epilogue (tcgen05.ld
 //               of the accumulator, coalesced f32 stores of Y).
@@ -46,7 +46,7 @@ constexpr int BK = 64;    // k per operand stage: one 128-byte swizzle atom of b
 constexpr int RK = 256;   // k per raw weight stage: 8 Q8_0 blocks, 272 bytes per row
 constexpr int NSTAGE = 3;
 constexpr int NRAW = 2;
-constexpr int NCONV = 8;  // converter / epilogue warps
+constexpr int NCONV = 16;  // converter / epilogue warps
 constexpr int NTHREADS = (2 + NCONV) * 32;
 constexpr uint32_t A_BYTES = BM * BK * 2;       // 16 KB
 constexpr uint32_t B_BYTES = BT * BK * 2;       // 32 KB
@@ -56,7 +56,9 @@ constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + NSTAGE * A_BYTES;
 constexpr uint32_t OFF_RAW = OFF_B + NSTAGE * B_BYTES;
 constexpr uint32_t OFF_BAR = OFF_RAW + NRAW * RAW_BYTES;
-constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
+constexpr uint32_t OFF_PARTS = OFF_BAR + 256;  // slot list of a split tile's parts
+constexpr int MAX_PARTS = 128;
+constexpr uint32_t SMEM_BYTES = OFF_PARTS + MAX_PARTS * 4 + 1024;  // + alignment slack
 constexpr uint32_t TMEM_COLS = 256;
 
 QG_DEVICE void gemm_status(unsigned int bits) { atomicOr(&g_qg_status_gemm, bits); }
@@ -131,9 +133,12 @@ __host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
 
 // ---- abort-aware bounded waits -------------------------------------------------------------
 QG_DEVICE bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
-  for (uint32_t i = 0; i < QG_WAIT_LIMIT; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 63u && *abort_flag) return false;
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > QG_WAIT_NS) break;
   }
   *abort_flag = 1;
   gemm_status(QG_STATUS_BIT_TIMEOUT);
@@ -162,43 +167,46 @@ QG_DEVICE int range_owner(long long p, long long total, int G) {
   return static_cast<int>(((p + 1) * G + total - 1) / total - 1);
 }
 
-// Decode 32 Q8_0 weights (one block) from the raw stage into the A slot: row `row`, k
-// offset 32 * blk within the 64-k stage.
-QG_DEVICE void convert_block(uint32_t raw_blk, uint32_t a_slot, int row, int blk) {
+// Decode 16 Q8_0 weights (half hb & 1 of block hb >> 1 of the 64-k stage `sub`) of one row
+// from the raw stage into the A slot.  raw_row: shared address of the row's 272 raw bytes;
+// a_row: shared address of the row in the A slot (128 bytes, 16-byte chunks swizzled by
+// row & 7).  The 16 code bytes are fetched with two aligned 16-byte loads (eight lanes of
+// consecutive rows hit eight different bank groups: the raw row pitch is 17 chunks).
+QG_DEVICE void convert_half(uint32_t raw_row, int sub, int hb, uint32_t a_row, int row) {
+  const uint32_t blk = raw_row + 68u * static_cast<uint32_t>(sub) + 34u * static_cast<uint32_t>(hb >> 1);
   uint32_t d16;
-  QG_LDS16(raw_blk, 0, d16);
+  QG_LDS16(blk, 0, d16);
   const float d = h2f(d16);
-  const uint32_t a = raw_blk + 2u, b = a & ~3u, sh = (a & 3u) * 8u;
-  uint32_t w[9];
-  QG_LDS32(b, 0, w[0]);
-  QG_LDS32(b, 4, w[1]);
-  QG_LDS32(b, 8, w[2]);
-  QG_LDS32(b, 12, w[3]);
-  QG_LDS32(b, 16, w[4]);
-  QG_LDS32(b, 20, w[5]);
-  QG_LDS32(b, 24, w[6]);
-  QG_LDS32(b, 28, w[7]);
-  QG_LDS32(b, 32, w[8]);
+  const uint32_t o = blk + 2u + 16u * static_cast<uint32_t>(hb & 1);
+  const uint32_t a16 = o & ~15u, off = o & 15u;
+  const uint4 v0 = lds_v4(a16), v1 = lds_v4(a16 + 16u);
+  const uint64_t q0 = (static_cast<uint64_t>(v0.y) << 32) | v0.x, q1 = (static_cast<uint64_t>(v0.w) << 32) | v0.z;
+  const uint64_t q2 = (static_cast<uint64_t>(v1.y) << 32) | v1.x, q3 = (static_cast<uint64_t>(v1.w) << 32) | v1.z;
+  const bool hi8 = off >= 8u;
+  const uint32_t sh = (off & 7u) * 8u;
+  const uint64_t l0 = hi8 ? q1 : q0, l1 = hi8 ? q2 : q1, l2 = hi8 ? q3 : q2;
+  const uint64_t lo = sh ? (l0 >> sh) | (l1 << (64u - sh)) : l0;
+  const uint64_t hi = sh ? (l1 >> sh) | (l2 << (64u - sh)) : l1;
+  const uint32_t cw[4] = {static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32), static_cast<uint32_t>(hi),
+                          static_cast<uint32_t>(hi >> 32)};
   const f2 d2 = mk2(d, d);
-  const f2 off = mk2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
-  const uint32_t row_base = a_slot + static_cast<uint32_t>(row) * 128u;
+  const f2 bias = mk2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {  // 16-byte chunk: 8 weights = 2 code words
-    uint32_t o[4];
+  for (int c = 0; c < 2; ++c) {  // two 16-byte chunks of 8 weights
+    uint32_t outw[4];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const uint32_t cw = __funnelshift_r(w[2 * c + h], w[2 * c + h + 1], sh) ^ 0x80808080u;
-      const f2 q01 = add2(mk2(magic_byte(cw, 0), magic_byte(cw, 1)), off);
-      const f2 q23 = add2(mk2(magic_byte(cw, 2), magic_byte(cw, 3)), off);
-      const f2 w01 = mul2(q01, d2), w23 = mul2(q23, d2);
+      const uint32_t word = cw[2 * c + h] ^ 0x80808080u;
+      const f2 w01 = mul2(add2(mk2(magic_byte(word, 0), magic_byte(word, 1)), bias), d2);
+      const f2 w23 = mul2(add2(mk2(magic_byte(word, 2), magic_byte(word, 3)), bias), d2);
       const __nv_bfloat162 b01 = __floats2bfloat162_rn(w01.x, w01.y);
       const __nv_bfloat162 b23 = __floats2bfloat162_rn(w23.x, w23.y);
-      o[2 * h] = *reinterpret_cast<const uint32_t *>(&b01);
-      o[2 * h + 1] = *reinterpret_cast<const uint32_t *>(&b23);
+      outw[2 * h] = *reinterpret_cast<const uint32_t *>(&b01);
+      outw[2 * h + 1] = *reinterpret_cast<const uint32_t *>(&b23);
     }
-    const uint32_t chunk = static_cast<uint32_t>((blk * 4 + c) ^ (row & 7));
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_base + chunk * 16u), "r"(o[0]), "r"(o[1]),
-                 "r"(o[2]), "r"(o[3])
+    const uint32_t chunk = static_cast<uint32_t>((2 * hb + c) ^ (row & 7));
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a_row + chunk * 16u), "r"(outw[0]), "r"(outw[1]),
+                 "r"(outw[2]), "r"(outw[3])
                  : "memory");
   }
 }
@@ -217,6 +225,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile unsigned int *s_last = reinterpret_cast<volatile unsigned int *>(tmem_slot + 2);
+  volatile int *s_nparts = reinterpret_cast<volatile int *>(tmem_slot + 3);
+  int *s_parts = reinterpret_cast<int *>(smem + OFF_PARTS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = static_cast<int>(gridDim.x);
@@ -241,6 +251,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();
+  pdl_launch_dependents();
   const uint32_t tmem = *tmem_slot;
 
   const uint32_t sA = smem_u32(smem + OFF_A), sB = smem_u32(smem + OFF_B), sRaw = smem_u32(smem + OFF_RAW);
@@ -325,10 +337,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     // ---------------- converters, then epilogue ----------------
-    const int ct = threadIdx.x - 64;  // 0 .. 255
-    const int crow = ct >> 1, cblk = ct & 1;
-    const int q = warp & 3;           // TMEM lane quarter this warp may read
-    const int half = (warp - 2) >> 2; // which 128 accumulator columns
+    const int ct = threadIdx.x - 64;          // 0 .. NCONV * 32 - 1
+    const int crow = 8 * (ct >> 5) + (lane & 7);  // weight row this thread converts
+    const int chb = lane >> 3;                   // its 16-weight quarter of the 64-k stage
+    const int q = warp & 3;                      // TMEM lane quarter this warp may read
+    const int cgrp = (warp - 2) >> 2;            // which 64 accumulator columns
     long long it = 0, rit = 0;
     int si = 0;
     bool ok = true;
@@ -349,9 +362,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ok = false;
             break;
           }
-          const uint32_t raw_blk = sRaw + r * RAW_BYTES + static_cast<uint32_t>(crow) * RAW_ROW +
-                                   static_cast<uint32_t>(sub * 2 + cblk) * 34u;
-          convert_block(raw_blk, sA + s * A_BYTES, crow, cblk);
+          convert_half(sRaw + r * RAW_BYTES + static_cast<uint32_t>(crow) * RAW_ROW, sub, chb,
+                       sA + s * A_BYTES + static_cast<uint32_t>(crow) * 128u, crow);
           fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
           __syncwarp();
           if (lane == 0) mbar_arrive(&full[s]);
@@ -373,8 +385,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!whole) slot = 2 * static_cast<int>(blockIdx.x) + (beg < static_cast<long long>(tile) * a.KS ? 1 : 0);
       float *dst = whole ? a.y : a.part + static_cast<size_t>(slot) * BT * BM;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        const int col0 = half * 128 + cc * 32;
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col0 = cgrp * 64 + cc * 32;
         float v[32];
         tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(col0), v);
         if (whole) {
@@ -399,28 +411,66 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const long long ts = static_cast<long long>(tile) * a.KS, te = ts + a.KS;
           const int bf = range_owner(ts, a.total, G), bl = range_owner(te - 1, a.total, G);
           int parts = 0;
-          for (int bp = bf; bp <= bl; ++bp)
-            if (range_start(bp, a.total, G) < range_start(bp + 1, a.total, G)) ++parts;
+          for (int bp = bf; bp <= bl; ++bp) {
+            const long long sbp = range_start(bp, a.total, G);
+            if (sbp < range_start(bp + 1, a.total, G)) {
+              if (parts < MAX_PARTS) s_parts[parts] = 2 * bp + (sbp < ts ? 1 : 0);
+              ++parts;
+            }
+          }
           const unsigned int old = atomicAdd(&a.cnt[tile], 1u);
           *s_last = (old + 1u == static_cast<unsigned int>(parts)) ? 1u : 0u;
+          *s_nparts = parts;
         }
         named_bar_sync(1, NCONV * 32);
         if (*s_last) {
           __threadfence();
-          const long long ts = static_cast<long long>(tile) * a.KS, te = ts + a.KS;
-          const int bf = range_owner(ts, a.total, G), bl = range_owner(te - 1, a.total, G);
-          const int mm = ct & (BM - 1), c0 = (ct >> 7) * (BT / 2);
-          const int mg = mt * BM + mm;
-          for (int c = c0; c < c0 + BT / 2; ++c) {
-            const int t = tt * BT + c;
-            float sum = 0.f;
-            for (int bp = bf; bp <= bl; ++bp) {
-              const long long sbp = range_start(bp, a.total, G);
-              if (sbp >= range_start(bp + 1, a.total, G)) continue;
-              const int sl = 2 * bp + (sbp < ts ? 1 : 0);
-              sum += __ldcg(a.part + (static_cast<size_t>(sl) * BT + c) * BM + mm);
+          const int parts = *s_nparts;
+          // thread: rows 4 m4 .. 4 m4 + 3, columns cs + NCONV j, in two batches of 8 columns
+          // (8 independent float4 loads in flight per part)
+          const int m4 = ct & 31, cs = ct >> 5;
+          constexpr int NJ = BT / NCONV, NB = 8;
+          const int mg = mt * BM + 4 * m4;
+#pragma unroll 1
+          for (int j0 = 0; j0 < NJ; j0 += NB) {
+            float4 acc[NB];
+#pragma unroll
+            for (int j = 0; j < NB; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int pi = 0; pi < parts; ++pi) {
+              int sl;
+              if (pi < MAX_PARTS) {
+                sl = s_parts[pi];
+              } else {  // more parts than the list holds: recompute this one
+                const long long ts = static_cast<long long>(tile) * a.KS;
+                int bp = range_owner(ts, a.total, G), seen = -1;
+                for (;; ++bp)
+                  if (range_start(bp, a.total, G) < range_start(bp + 1, a.total, G) && ++seen == pi) break;
+                sl = 2 * bp + (range_start(bp, a.total, G) < ts ? 1 : 0);
+              }
+              const float4 *pp = reinterpret_cast<const float4 *>(a.part + static_cast<size_t>(sl) * BT * BM);
+#pragma unroll
+              for (int j = 0; j < NB; ++j) {
+                const float4 v = __ldcg(pp + (cs + NCONV * (j0 + j)) * (BM / 4) + m4);
+                acc[j].x += v.x;
+                acc[j].y += v.y;
+                acc[j].z += v.z;
+                acc[j].w += v.w;
+              }
             }
-            if (t < a.T && mg < a.M) a.y[static_cast<size_t>(t) * a.M + mg] = sum;
+#pragma unroll
+            for (int j = 0; j < NB; ++j) {
+              const int t = tt * BT + cs + NCONV * (j0 + j);
+              if (t >= a.T) continue;
+              float *yr = a.y + static_cast<size_t>(t) * a.M;
+              if (mg + 3 < a.M && (a.M & 3) == 0) {
+                *reinterpret_cast<float4 *>(yr + mg) = acc[j];
+              } else {
+                if (mg < a.M) yr[mg] = acc[j].x;
+                if (mg + 1 < a.M) yr[mg + 1] = acc[j].y;
+                if (mg + 2 < a.M) yr[mg + 2] = acc[j].z;
+                if (mg + 3 < a.M) yr[mg + 3] = acc[j].w;
+              }
+            }
           }
           named_bar_sync(1, NCONV * 32);
           if (ct == 0) a.cnt[tile] = 0u;
@@ -440,6 +490,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // f32 -> bf16 (round to nearest even) copy of X, and zeroed tile counters
 __global__ void qgemm_prep_kernel(const float4 *__restrict__ x, uint2 *__restrict__ xb, long long n4,
                                   unsigned int *cnt, int ncnt) {
+  pdl_wait();
+  pdl_launch_dependents();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
     const float4 v = __ldg(x + i);
@@ -518,9 +570,9 @@ qg_status gemm_tc(const void *w, const float *x, float *y, int64_t M, int64_t N,
   }
   const long long n4 = T * N / 4;
   const int pb = static_cast<int>(std::min<long long>(4LL * dev.sms, (n4 + 255) / 256));
-  qgemm_prep_kernel<<<std::max(pb, 1), 256, 0, s>>>(reinterpret_cast<const float4 *>(x), reinterpret_cast<uint2 *>(xb),
-                                                   n4, cnt, p.n_mt * p.n_tt);
-  if (cudaGetLastError() != cudaSuccess) return QG_ECUDA;
+  if (qg::launch_pdl(qgemm_prep_kernel, dim3(std::max(pb, 1)), dim3(256), 0, s, reinterpret_cast<const float4 *>(x),
+                     reinterpret_cast<uint2 *>(xb), n4, cnt, p.n_mt * p.n_tt) != cudaSuccess)
+    return QG_ECUDA;
 
   GemmArgs a{};
   a.y = y;
@@ -534,7 +586,8 @@ qg_status gemm_tc(const void *w, const float *x, float *y, int64_t M, int64_t N,
   a.KS = p.KS;
   a.total = p.total;
   if (!qg::set_smem_attr(reinterpret_cast<const void *>(qgemm_q8_0_kernel), SMEM_BYTES)) return QG_ECUDA;
-  qgemm_q8_0_kernel<<<p.G, NTHREADS, SMEM_BYTES, s>>>(wmap, xmap, a);
+  if (qg::launch_pdl(qgemm_q8_0_kernel, dim3(p.G), dim3(NTHREADS), SMEM_BYTES, s, wmap, xmap, a) != cudaSuccess)
+    return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 

@@ -5,18 +5,20 @@
 // diskformer package), f32 activations and f32 accumulation.
 //
 // Design (persistent CTAs, one per SM; every warp runs its own pipeline):
-//   - each warp owns row blocks of 4 rows and NS shared-memory slots with one mbarrier
-//     each.  Lane 0 issues the warp's next stages ahead with 1-D bulk copies (the TMA
-//     engine, cp.async.bulk): a stage is the warp's 4 rows times one K chunk, one copy per
-//     row segment (or one copy for 4 whole rows, which are contiguous in the raw layout).
-//     No producer warp: on this GPU a single issuing thread caps a CTA's bulk-copy rate well
-//     below HBM speed, while per-warp issue streams at full bandwidth.
+//   - each warp owns row blocks (2 rows for one token, 4 when several token columns share
+//     every decoded weight) and NS shared-memory slots with one mbarrier each.  The warp
+//     issues its next stages ahead with 1-D bulk copies (the TMA engine, cp.async.bulk): a
+//     stage is the block's whole rows in one copy (they are contiguous in the raw layout)
+//     or one copy per row segment of at least 2 KB.  Copies that small stream at full
+//     speed; much smaller ones are capped by the copy engine's per-copy rate.  No producer
+//     warp: a single issuing thread caps a CTA's bulk-copy rate well below HBM speed, while
+//     per-warp issue streams at full bandwidth.
 //   - the warp decodes its rows straight from the raw blocks in shared memory
-//     (qg_decode.cuh), reusing every activation load for its 4 rows, and keeps the
+//     (qg_decode.cuh), reusing every activation load for the block's rows, and keeps the
 //     accumulators in registers across the row's chunks.
 //   - activations: when all T rows fit in shared memory they are loaded once (2-D tensor
 //     copies with the 128-byte swizzle); otherwise they come in double-buffered K chunks
-//     that every warp walks in step, Y accumulating across chunks.
+//     that every warp walks in step, chunk partial sums kept in shared memory.
 //   - with few rows, KW warps split a row block's chunks and meet at a named barrier to sum
 //     their partials in a fixed order (deterministic).
 //   - every weight byte crosses HBM once per call, whatever T is.
@@ -43,11 +45,11 @@ struct GemvArgs {
   int KC;            // elements per weight chunk (multiple of SG)
   int nchunks;       // chunks per row
   int xR;            // activation rows (32 floats) per token in one buffer
-  int rblocks;       // row blocks of 4 rows
+  int rblocks;       // row blocks (2 rows for one token, else 4)
   int max_kw;        // most warps that may split one row block (mode 0; <= nchunks)
   int NS;            // slots per warp
   int stage_bytes;   // bytes per slot
-  int seg_slot;      // bytes per row segment inside a slot; 0: 4 whole rows in one copy
+  int seg_slot;      // bytes per row segment inside a slot; 0: the block's whole rows in one copy
   int box_rows;      // rows per activation tensor copy
   int maxq;          // most row blocks of one warp (mode 1 partial sums)
   uint32_t off_x, off_ring, off_red, off_part;
@@ -61,15 +63,23 @@ struct Cursor {
   int q, c;
 };
 
+// Rows per row block: 2 for one token (so that a stage of whole rows stays one large copy
+// with 16 warps), 4 when several token columns share every decoded weight.
+template <int TT>
+__host__ __device__ constexpr int rows_per_block() {
+  return TT == 1 ? 2 : 4;
+}
+
 template <int QT, int TT, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant__ CUtensorMap xmap, const GemvArgs a) {
   using D = Dec<QT>;
+  constexpr int RR = rows_per_block<TT>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *wbar = reinterpret_cast<uint64_t *>(smem);  // [NW][kMaxNS]
   uint64_t *xfull = wbar + NW * kMaxNS;                  // [2]
-  float *red = reinterpret_cast<float *>(smem + a.off_red);    // [2][NW][4][TT]
-  float *part = reinterpret_cast<float *>(smem + a.off_part);  // [NW][maxq][4][TT] (mode 1)
+  float *red = reinterpret_cast<float *>(smem + a.off_red);    // [2][NW][RR][TT]
+  float *part = reinterpret_cast<float *>(smem + a.off_part);  // [NW][maxq][RR][TT] (mode 1)
   uint8_t *xs = smem + a.off_x;
   uint8_t *ring = smem + a.off_ring;
 
@@ -94,6 +104,10 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
     mbar_init(&xfull[0], 1);
     mbar_init(&xfull[1], 1);
     fence_mbar_init();
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
     load_x(xs, &xmap, a.T, a.N, 0, a.xR, a.box_rows, &xfull[0]);
     if (a.mode == 1 && a.nchunks > 1) load_x(xs + a.xbuf_bytes, &xmap, a.T, a.N, 1, a.xR, a.box_rows, &xfull[1]);
   }
@@ -124,37 +138,29 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
   uint8_t *wring = ring + warp * a.NS * a.stage_bytes;
   const uint32_t wring_s = smem_u32(wring);
 
-  // Issue the stage of item u into slot s.  Lane r copies row r's segment (lane 0 copies 4
-  // whole rows at once); the byte count goes to the slot's mbarrier before any copy starts.
+  // Issue the stage of item u into slot s: lane r copies row r's segment (lane 0 copies 4
+  // whole rows at once when the stage holds whole rows); the byte count goes to the slot's
+  // mbarrier before any copy starts.
   const bool pad_rows = a.seg_slot != 0;
   auto issue = [&](Cursor u, int s) {
     const long long rb = rb_of(u);
-    const int nr = (my_rbs == 0) ? 0 : static_cast<int>(max(0LL, min(4LL, a.M - rb * 4)));
+    const int nr = (my_rbs == 0) ? 0 : static_cast<int>(max(0LL, min(static_cast<long long>(RR), a.M - rb * RR)));
     uint8_t *st = wring + s * a.stage_bytes;
-    uint64_t *bar = &wbar[warp * kMaxNS + s];
     uintptr_t src = 0;
     uint32_t n = 0;
     uint8_t *dst = st;
     if (!pad_rows) {
       if (lane == 0) {
-        src = wbase + static_cast<uintptr_t>(rb * 4 * a.row_bytes);
+        src = wbase + static_cast<uintptr_t>(rb * RR * a.row_bytes);
         n = static_cast<uint32_t>(nr * a.row_bytes);
       }
     } else if (lane < nr) {
       const int kel = min(a.N - u.c * a.KC, a.KC);
       n = static_cast<uint32_t>(kel / D::QK) * D::BB;
-      src = wbase + static_cast<uintptr_t>((rb * 4 + lane) * a.row_bytes + u.c * chunk_bytes);
+      src = wbase + static_cast<uintptr_t>((rb * RR + lane) * a.row_bytes + u.c * chunk_bytes);
       dst = st + lane * a.seg_slot;
     }
-    uint32_t nb = 0;
-    if (n) nb = stage_copy(dst, src, n, mend, bar, false);  // size, and tail bytes past mend
-    const uint32_t tx = __reduce_add_sync(0xFFFFFFFFu, nb);
-    if (lane == 0) mbar_arrive_expect_tx(bar, tx);
-    __syncwarp();
-    if (nb) {
-      fence_proxy_async_smem();  // the slot's previous bytes were read through the generic proxy
-      bulk_g2s(dst, reinterpret_cast<const void *>(src & ~static_cast<uintptr_t>(15)), nb, bar);
-    }
+    warp_bulk_copies(dst, src, n, mend, &wbar[warp * kMaxNS + s], lane);
   };
 
   // prologue: the first NS - 1 items
@@ -175,8 +181,8 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
 
   bool ok = true;
   if (!mbar_wait(&xfull[0], 0)) ok = false;
-  float acc1[4];
-  f2 acc2[4][TT];
+  float acc1[RR];
+  f2 acc2[RR][TT];
   Cursor cc = first();
   int cs = 0, cround = 0, consumed = 0;
   int cur_xc = 0;  // activation chunk the warp is on (mode 1)
@@ -200,7 +206,7 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
     const bool last_chunk = (a.mode == 1) || (cc.c + KW >= a.nchunks);
     if (first_chunk) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < RR; ++r) {
         acc1[r] = 0.f;
 #pragma unroll
         for (int t = 0; t < TT; ++t) acc2[r][t] = mk2(0.f, 0.f);
@@ -211,13 +217,13 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
       const int kel = min(a.N - cc.c * a.KC, a.KC);
       const int gcount = (kel + D::SG - 1) / D::SG;
       const uint32_t st = wring_s + static_cast<uint32_t>(cs * a.stage_bytes);
-      uint32_t wrow[4];
+      uint32_t wrow[RR];
       {
         // low 32 bits suffice: only the address modulo 16 matters
-        const uint32_t r0 = static_cast<uint32_t>(wbase) + static_cast<uint32_t>(rb * 4) * static_cast<uint32_t>(a.row_bytes);
+        const uint32_t r0 = static_cast<uint32_t>(wbase) + static_cast<uint32_t>(rb * RR) * static_cast<uint32_t>(a.row_bytes);
         const uint32_t cb = static_cast<uint32_t>(cc.c) * static_cast<uint32_t>(chunk_bytes);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < RR; ++r) {
           if (!pad_rows)
             wrow[r] = st + (r0 & 15u) + static_cast<uint32_t>(r) * static_cast<uint32_t>(a.row_bytes) + wo;
           else
@@ -237,27 +243,27 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
 #pragma unroll
           for (int ch = 0; ch < D::NCH; ++ch) xc[ch] = lds_f4(xg + xo[ch]);
           const float aux = D::xaux(xc);
-          typename D::U u[4];
+          typename D::U u[RR];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) u[r] = D::load(wrow[r] + goff, lane);
+          for (int r = 0; r < RR; ++r) u[r] = D::load(wrow[r] + goff, lane);
 #pragma unroll
-          for (int r = 0; r < 4; ++r) acc1[r] += D::dot1(u[r], xc, aux);
+          for (int r = 0; r < RR; ++r) acc1[r] += D::dot1(u[r], xc, aux);
         } else {
-          typename D::U u[4];
+          typename D::U u[RR];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) u[r] = D::load(wrow[r] + goff, lane);
+          for (int r = 0; r < RR; ++r) u[r] = D::load(wrow[r] + goff, lane);
 #pragma unroll
           for (int ch = 0; ch < D::NCH; ++ch) {
-            f2 w01[4], w23[4];
+            f2 w01[RR], w23[RR];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) D::weights(u[r], ch, w01[r], w23[r]);
+            for (int r = 0; r < RR; ++r) D::weights(u[r], ch, w01[r], w23[r]);
 #pragma unroll
             for (int t = 0; t < TT; ++t) {
               if (t < a.T) {
                 const float4 xv = lds_f4(xg + static_cast<uint32_t>(t * xbytes_token) + xo[ch]);
                 const f2 x01 = mk2(xv.x, xv.y), x23 = mk2(xv.z, xv.w);
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
+                for (int r = 0; r < RR; ++r) {
                   acc2[r][t] = fma2(w01[r], x01, acc2[r][t]);
                   acc2[r][t] = fma2(w23[r], x23, acc2[r][t]);
                 }
@@ -277,11 +283,11 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
     if (last_chunk && my_rbs > 0) {
       // the 4 x TT row sums, reduce-scattered over the warp (each lane ends up owning one or
       // two of them)
-      constexpr int NV = 4 * TT;
+      constexpr int NV = RR * TT;
       constexpr int NH = NV == 64 ? 2 : 1;
       float v[NV];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < RR; ++r)
 #pragma unroll
         for (int t = 0; t < TT; ++t) v[r * TT + t] = (TT == 1) ? acc1[r] : acc2[r][t].x + acc2[r][t].y;
       reduce_scatter<NV>(v, lane);
@@ -301,7 +307,7 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
             if (cc.c > 0) val += pacc[idx];
             if (!final_chunk) pacc[idx] = val;
           }
-          const long long row = rb * 4 + r;
+          const long long row = rb * RR + r;
           if (own && final_chunk && ok && t < a.T && row < a.M) a.y[static_cast<long long>(t) * a.M + row] = val;
         }
       } else {
@@ -316,7 +322,7 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
             const int r = idx / TT, t = idx - r * TT;
             float sum = 0.f;
             for (int k = 0; k < KW; ++k) sum += base[k * NV + idx];
-            const long long row = rb * 4 + r;
+            const long long row = rb * RR + r;
             if (ok && t < a.T && row < a.M) a.y[static_cast<long long>(t) * a.M + row] = sum;
           }
         }
@@ -346,30 +352,39 @@ qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N
   const long long row_bytes = N / D::QK * D::BB;
   const long long budget = dev.smem_optin - 4096;
   const uint32_t hdr = 1024;
-  const uint32_t red_bytes = 2 * NW * 4 * TT * 4;
+  constexpr int RR = rows_per_block<TT>();
+  const uint32_t red_bytes = 2 * NW * RR * TT * 4;
   const long long xres = ((static_cast<long long>(T) * ngroups * D::SG * 4 + 1023) / 1024) * 1024;
 
   GemvArgs a{};
-  const long long rblocks = (M + 3) / 4;
+  const long long rblocks = (M + RR - 1) / RR;
   const long long rb_per_cta = (rblocks + dev.sms - 1) / dev.sms;
   // activations resident (mode 0) when that still leaves the warps a ring of >= 48 KB
   int mode = (xres + 48 * 1024 <= budget - hdr - red_bytes - 1024) ? 0 : 1;
   int gpc = 0, NS = 0, seg_slot = 0;
   long long stage = 0, part_bytes = 0;
   uint32_t xbuf = 0;
+  // Bulk copies of 2 KB or more stream at full speed; much smaller ones are limited by the
+  // copy engine's per-copy rate.  One token: stages of whole rows (one copy) when two fit in
+  // a warp's share of the ring, else row segments of at least 2 KB.  Several tokens: stages
+  // of ~2-6 KB with three or more slots per warp.
+  const int gpc_floor = (TT == 1) ? std::min(ngroups, (2048 + D::GB - 1) / D::GB) : 1;
+  auto seg_for = [&](int g) { return static_cast<int>(((static_cast<long long>(g) * D::GB + 15) & ~15LL) + 32); };
   auto plan_ring = [&](long long ring_avail) {
-    // stages of ~4-6 KB: 4 whole rows when they fit, else 4 row segments of gpc groups
-    const long long target = std::max<long long>(2048, std::min<long long>(6144, ring_avail / (3LL * NW)));
-    const long long whole = ((4 * row_bytes + 15) & ~15LL) + 32;
+    const long long tmax = (TT == 1) ? 16384 : 6144;
+    const long long target = std::max<long long>(2048, std::min<long long>(tmax, ring_avail / ((TT == 1 ? 2LL : 3LL) * NW)));
+    const long long whole = ((RR * row_bytes + 15) & ~15LL) + 32;
     if (mode == 0 && whole <= target) {
       gpc = ngroups;
       seg_slot = 0;
       stage = whole;
     } else {
-      gpc = static_cast<int>(std::max<long long>(1, target / (4LL * D::GB)));
-      gpc = std::min(gpc, ngroups);
-      seg_slot = static_cast<int>(((static_cast<long long>(gpc) * D::GB + 15) & ~15LL) + 32);
-      stage = 4LL * seg_slot;
+      int gmax = static_cast<int>(std::max<long long>(1, (target / RR - 32) / D::GB));
+      gmax = std::max(std::min(gmax, ngroups), gpc_floor);
+      const int nch = (ngroups + gmax - 1) / gmax;
+      gpc = (ngroups + nch - 1) / nch;  // even chunks
+      seg_slot = seg_for(gpc);
+      stage = static_cast<long long>(RR) * seg_slot;
     }
     NS = static_cast<int>(std::min<long long>(kMaxNS, ring_avail / (static_cast<long long>(NW) * stage)));
   };
@@ -384,13 +399,13 @@ qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N
     int g = static_cast<int>(std::max<long long>(1, (40 * 1024) / per_group));
     g = std::min(g, ngroups);
     // per-warp partial sums of its row blocks across chunks
-    part_bytes = ((static_cast<long long>(NW) * ((rb_per_cta + NW - 1) / NW) * 4 * TT * 4) + 1023) & ~1023LL;
+    part_bytes = ((static_cast<long long>(NW) * ((rb_per_cta + NW - 1) / NW) * RR * TT * 4) + 1023) & ~1023LL;
     while (true) {
       xbuf = static_cast<uint32_t>(((per_group * g + 1023) / 1024) * 1024);
       const long long ring_avail = budget - hdr - red_bytes - 2LL * xbuf - part_bytes - 1024;
       gpc = g;
-      seg_slot = static_cast<int>(((static_cast<long long>(gpc) * D::GB + 15) & ~15LL) + 32);
-      stage = 4LL * seg_slot;
+      seg_slot = seg_for(gpc);
+      stage = static_cast<long long>(RR) * seg_slot;
       NS = ring_avail > 0 ? static_cast<int>(std::min<long long>(kMaxNS, ring_avail / (static_cast<long long>(NW) * stage)))
                           : 0;
       if (NS >= 3 || g == 1) break;
@@ -400,15 +415,17 @@ qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N
   }
   int nchunks = (ngroups + gpc - 1) / gpc;
   // when a CTA gets fewer row blocks than warps its warps split K: make sure there are
-  // enough chunks for that (stages then shrink to a group or two)
+  // enough chunks for that (but keep segments at the copy-size floor)
   if (mode == 0 && rb_per_cta < NW) {
     const int want_kw = static_cast<int>(std::min<long long>(NW, NW / std::max<long long>(1, rb_per_cta)));
-    while (gpc > 1 && (ngroups + gpc - 1) / gpc < want_kw) {
-      gpc = std::max(1, gpc / 2);
-      seg_slot = static_cast<int>(((static_cast<long long>(gpc) * D::GB + 15) & ~15LL) + 32);
-      stage = 4LL * seg_slot;
+    while (gpc > gpc_floor && (ngroups + gpc - 1) / gpc < want_kw) {
+      gpc = std::max(gpc_floor, gpc / 2);
+      seg_slot = seg_for(gpc);
+      stage = static_cast<long long>(RR) * seg_slot;
     }
     nchunks = (ngroups + gpc - 1) / gpc;
+    NS = static_cast<int>(std::min<long long>(kMaxNS, (budget - hdr - red_bytes - xbuf - 1024) / (static_cast<long long>(NW) * stage)));
+    if (NS < 2) return QG_EUNSUPPORTED;
   }
   a.w = static_cast<const uint8_t *>(w);
   a.y = y;
@@ -454,7 +471,7 @@ qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N
   auto kern = qgemv_kernel<QT, TT, NW>;
   if (!qg::set_smem_attr(reinterpret_cast<const void *>(kern), smem)) return QG_ECUDA;
   const int grid = static_cast<int>(std::min<long long>(rblocks, dev.sms));
-  kern<<<grid, NW * 32, smem, stream>>>(map, a);
+  if (qg::launch_pdl(kern, dim3(grid), dim3(NW * 32), smem, stream, map, a) != cudaSuccess) return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 

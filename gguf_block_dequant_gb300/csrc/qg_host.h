@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/ggufdq.h"
 
 namespace qg {
@@ -22,6 +24,24 @@ const DeviceInfo &device_info();
 bool set_smem_attr(const void *func, uint32_t bytes);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Launch with programmatic stream serialization allowed: the kernel may begin while its
+// predecessor in the stream drains; it synchronises with griddepcontrol.wait (pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // dense GEMV entry shared by qgemv_* / qgemv_t / qgemm (small T) / MoE helpers
 qg_status gemv_dispatch(int type, const void *w, const float *x, float *y, int64_t M, int64_t N, int T,

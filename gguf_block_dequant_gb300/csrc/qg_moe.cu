@@ -100,10 +100,13 @@ QG_DEVICE void topk_token(const float *l, int E, int k, int lane, int32_t *ids, 
 __global__ void __launch_bounds__(kRouterWarps * 32) moe_router_kernel(const float *__restrict__ xn,
                                                                         const float *__restrict__ wr, int T, int H,
                                                                         int E, int k, float *logits, int32_t *ids,
-                                                                        float *weights, unsigned int *ticket) {
+                                                                        float *weights, unsigned int *ticket,
+                                                                        int do_topk) {
   __shared__ float part[kRouterWarps][kRouterTB];
   __shared__ unsigned int s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_launch_dependents();
   const int e = blockIdx.x;
   const int t0 = blockIdx.y * kRouterTB;
   const int nt = min(kRouterTB, T - t0);
@@ -139,6 +142,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32) moe_router_kernel(const flo
     for (int w = 0; w < kRouterWarps; ++w) s += part[w][threadIdx.x];
     logits[static_cast<size_t>(t0 + threadIdx.x) * E + e] = s;
   }
+  if (!do_topk) return;
   // the last CTA of this token tile to finish takes the picks
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -181,6 +185,12 @@ struct MoeArgs {
   int KC, nchunks, NS, stage_bytes, seg_slot;
   int xrow_bytes;    // shared-memory bytes per token slot (whole groups of SG elements)
   int add_residual;
+  // gate/up kernel inside moe_layer: take the top-k picks from the router logits here
+  // (every CTA ranks the logits itself; CTA 0 also stores ids and weights)
+  int fuse_topk;
+  const float *logits;
+  int32_t *ids_out;
+  float *wts_out;
   uint32_t off_plan, off_x, off_ring;
 };
 
@@ -189,6 +199,8 @@ struct MoeArgs {
 // s_pairs[u_first[u] .. + u_cnt[u]) of one expert (at most TT pairs), slot u_slot[u].
 struct PlanSmem {
   int *s_id, *s_pairs, *u_slot, *u_first, *u_cnt, *s_cnt, *s_start, *s_ustart, *s_kv;
+  int32_t *tk_ids;  // fused top-k results [T][k]
+  float *tk_w;
 };
 
 QG_DEVICE PlanSmem plan_layout(uint8_t *base, int P, int T) {
@@ -211,11 +223,15 @@ QG_DEVICE PlanSmem plan_layout(uint8_t *base, int P, int T) {
   p.s_ustart = q;
   q += kMaxE + 1;
   p.s_kv = q;
+  q += T;
+  p.tk_ids = q;
+  q += P;
+  p.tk_w = reinterpret_cast<float *>(q);
   return p;
 }
 
 inline uint32_t plan_bytes(int P, int T) {
-  return static_cast<uint32_t>((5 * P + 3 * kMaxE + 1 + T) * 4 + 15) & ~15u;
+  return static_cast<uint32_t>((7 * P + 3 * kMaxE + 1 + T) * 4 + 15) & ~15u;
 }
 
 // Builds the grouping; returns the number of units.  Every thread of the CTA takes part.
@@ -223,8 +239,18 @@ template <int NW>
 QG_DEVICE int build_plan(const MoeArgs &a, int TT, const PlanSmem &p) {
   const int P = a.T * a.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (a.fuse_topk) {
+    for (int t = warp; t < a.T; t += NW)
+      topk_token(a.logits + static_cast<size_t>(t) * a.E, a.E, a.k, lane, p.tk_ids + t * a.k, p.tk_w + t * a.k);
+    __syncthreads();
+    if (blockIdx.x == 0)
+      for (int z = tid; z < P; z += NW * 32) {
+        a.ids_out[z] = p.tk_ids[z];
+        a.wts_out[z] = p.tk_w[z];
+      }
+  }
   for (int z = tid; z < P; z += NW * 32) {
-    const int e = __ldg(a.ids + z);
+    const int e = a.fuse_topk ? p.tk_ids[z] : __ldg(a.ids + z);
     bool ok = e >= 0 && e < a.E;
     if (ok) {
       const int s = a.slots ? __ldg(a.slots + e) : e;
@@ -344,6 +370,8 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
     for (int i = 0; i < NW * kMaxNS; ++i) mbar_init(&wbar[i], 1);
     fence_mbar_init();
   }
+  pdl_wait();
+  pdl_launch_dependents();
   const int nunits = build_plan<NW>(a, TT, pl);
 
   // pairs with a bad id: their act row is zero (gate/up); tokens without any valid pick keep
@@ -367,26 +395,10 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
   const int uA = static_cast<int>(rbA / a.nblk);
   const int uB = static_cast<int>((rbB - 1) / a.nblk);
 
-  // activations of the tokens this CTA needs
-  if constexpr (!DOWN) {
-    for (int t = 0; t < a.T; ++t)
-      copy_x_row(xs, t, a.xrow_bytes, a.xin + static_cast<size_t>(t) * a.K, a.K, threadIdx.x, NW * 32);
-  } else {
-    for (int u = uA; u <= uB; ++u)
-      for (int t = 0; t < pl.u_cnt[u]; ++t) {
-        const int z = pl.s_pairs[pl.u_first[u] + t];
-        copy_x_row(xs, (u - uA) * TT + t, a.xrow_bytes, a.xin + static_cast<size_t>(z) * a.K, a.K, threadIdx.x,
-                   NW * 32);
-      }
-  }
-  cp_async_wait_all();
-  __syncthreads();
-
   // ---- this warp's row blocks rbA + warp + i * NW, each in nchunks K chunks
   const int nrb = static_cast<int>(rbB - rbA);
   const int my_rbs = warp < nrb ? (nrb - warp + NW - 1) / NW : 0;
   const int n_items = my_rbs * a.nchunks;
-  if (n_items == 0) return;
   const long long chunk_bytes = static_cast<long long>(a.KC / D::QK) * D::BB;
   uint8_t *wring = ring + warp * a.NS * a.stage_bytes;
   const uint32_t wring_s = smem_u32(wring);
@@ -396,7 +408,6 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
     const long long rb = rbA + warp + static_cast<long long>(i) * NW;
     const int u = static_cast<int>(rb / a.nblk), p = static_cast<int>(rb - static_cast<long long>(u) * a.nblk);
     uint8_t *st = wring + s * a.stage_bytes;
-    uint64_t *bar = &wbar[warp * kMaxNS + s];
     uintptr_t src = 0;
     uint32_t n = 0;
     uint8_t *dst = st + lane * a.seg_slot;
@@ -412,19 +423,28 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
               static_cast<uintptr_t>(row) * a.row_bytes + static_cast<uintptr_t>(c) * chunk_bytes;
       }
     }
-    uint32_t nb = 0;
-    if (n) nb = stage_copy(dst, src, n, mend, bar, false);
-    const uint32_t tx = __reduce_add_sync(0xFFFFFFFFu, nb);
-    if (lane == 0) mbar_arrive_expect_tx(bar, tx);
-    __syncwarp();
-    if (nb) {
-      fence_proxy_async_smem();
-      bulk_g2s(dst, reinterpret_cast<const void *>(src & ~static_cast<uintptr_t>(15)), nb, bar);
-    }
+    warp_bulk_copies(dst, src, n, mend, &wbar[warp * kMaxNS + s], lane);
   };
 
   int issued = 0;
   for (; issued < a.NS - 1 && issued < n_items; ++issued) issue(issued, issued % a.NS);
+
+  // activations of the tokens this CTA needs (the first weight stages are already in flight)
+  if constexpr (!DOWN) {
+    for (int t = 0; t < a.T; ++t)
+      copy_x_row(xs, t, a.xrow_bytes, a.xin + static_cast<size_t>(t) * a.K, a.K, threadIdx.x, NW * 32);
+  } else {
+    for (int u = uA; u <= uB; ++u)
+      for (int t = 0; t < pl.u_cnt[u]; ++t) {
+        const int z = pl.s_pairs[pl.u_first[u] + t];
+        copy_x_row(xs, (u - uA) * TT + t, a.xrow_bytes, a.xin + static_cast<size_t>(z) * a.K, a.K, threadIdx.x,
+                   NW * 32);
+      }
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  if (n_items == 0) return;
 
   const uint32_t wo = static_cast<uint32_t>(D::woff(lane));
   uint32_t xo[D::NCH];
@@ -577,35 +597,43 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
             a.dn[static_cast<size_t>(z) * a.H + h0 + r] = v[hh];
           }
         }
-        __threadfence();
-        __syncwarp();
-        // lane t counts token t's pick for this row block; the pick that completes a token's
-        // k picks forms its combine
-        unsigned int last = 0;
-        int tok = 0;
-        if (lane < ucnt) {
-          tok = pl.s_pairs[pl.u_first[u] + lane] / a.k;
-          const unsigned int old = atomicAdd(&a.cnt[static_cast<size_t>(tok) * a.nblk + p], 1u);
-          last = (old + 1u == static_cast<unsigned int>(pl.s_kv[tok])) ? 1u : 0u;
-        }
-        unsigned int lastm = __ballot_sync(0xFFFFFFFFu, last != 0);
-        if (lastm) __threadfence();
-        while (lastm) {
-          const int src = __ffs(lastm) - 1;
-          lastm &= lastm - 1;
-          const int tk = __shfl_sync(0xFFFFFFFFu, tok, src);
-          const int h = h0 + lane;
-          if (lane < 4 && h < a.H) {
-            float sum = 0.f;
-            for (int j = 0; j < a.k; ++j) {
-              const int zj = tk * a.k + j;
-              if (pl.s_id[zj] >= 0) sum = fmaf(__ldg(a.wts + zj), __ldcg(a.dn + static_cast<size_t>(zj) * a.H + h), sum);
-            }
-            float *o = a.out + static_cast<size_t>(tk) * a.H + h;
-            if (ok) *o = a.add_residual ? *o + sum : sum;
+      }
+    }
+  }
+  if constexpr (DOWN) {
+    // one fence for all of this warp's dn values, then each (token, row block) pick is
+    // counted; the pick that completes a token's valid picks forms that token's combine
+    __threadfence();
+    __syncwarp();
+    for (int i = 0; i < my_rbs && ok; ++i) {
+      const long long rb = rbA + warp + static_cast<long long>(i) * NW;
+      const int u = static_cast<int>(rb / a.nblk), p = static_cast<int>(rb - static_cast<long long>(u) * a.nblk);
+      const int ucnt = pl.u_cnt[u];
+      const int h0 = 4 * p;
+      unsigned int last = 0;
+      int tok = 0;
+      if (lane < ucnt) {
+        tok = pl.s_pairs[pl.u_first[u] + lane] / a.k;
+        const unsigned int old = atomicAdd(&a.cnt[static_cast<size_t>(tok) * a.nblk + p], 1u);
+        last = (old + 1u == static_cast<unsigned int>(pl.s_kv[tok])) ? 1u : 0u;
+      }
+      unsigned int lastm = __ballot_sync(0xFFFFFFFFu, last != 0);
+      if (lastm) __threadfence();
+      while (lastm) {
+        const int src = __ffs(lastm) - 1;
+        lastm &= lastm - 1;
+        const int tk = __shfl_sync(0xFFFFFFFFu, tok, src);
+        const int h = h0 + lane;
+        if (lane < 4 && h < a.H) {
+          float sum = 0.f;
+          for (int j = 0; j < a.k; ++j) {
+            const int zj = tk * a.k + j;
+            if (pl.s_id[zj] >= 0) sum = fmaf(__ldg(a.wts + zj), __ldcg(a.dn + static_cast<size_t>(zj) * a.H + h), sum);
           }
-          if (lane == 0) a.cnt[static_cast<size_t>(tk) * a.nblk + p] = 0u;
+          float *o = a.out + static_cast<size_t>(tk) * a.H + h;
+          *o = a.add_residual ? *o + sum : sum;
         }
+        if (lane == 0) a.cnt[static_cast<size_t>(tk) * a.nblk + p] = 0u;
       }
     }
   }
@@ -645,7 +673,7 @@ qg_status check_common(int T, int k, int E, int H, int F) {
 }
 
 qg_status route_impl(const float *xn, const float *wr, int T, int H, int E, int k, int32_t *ids, float *weights,
-                     float *logits_out, void *ws, size_t ws_bytes, cudaStream_t s) {
+                     float *logits_out, void *ws, size_t ws_bytes, cudaStream_t s, int do_topk = 1) {
   if (!xn || !wr || !ids || !weights || !ws) return QG_EINVAL_PTR;
   if (T < 1 || k < 1 || k > kMaxK || E < k || E > kMaxE || H < 4 || H % 4) return QG_EINVAL_SHAPE;
   if (static_cast<long long>(T) * H > INT32_MAX || static_cast<long long>(T) * E > INT32_MAX) return QG_EINVAL_SHAPE;
@@ -656,8 +684,9 @@ qg_status route_impl(const float *xn, const float *wr, int T, int H, int E, int 
   float *logits = logits_out ? logits_out : reinterpret_cast<float *>(w + L.logits);
   const dim3 grid(E, (T + kRouterTB - 1) / kRouterTB);
   if (grid.y > 65535) return QG_EINVAL_SHAPE;
-  moe_router_kernel<<<grid, kRouterWarps * 32, 0, s>>>(xn, wr, T, H, E, k, logits, ids, weights,
-                                                     reinterpret_cast<unsigned int *>(w + L.ticket));
+  if (qg::launch_pdl(moe_router_kernel, grid, dim3(kRouterWarps * 32), 0, s, xn, wr, T, H, E, k, logits, ids, weights,
+                     reinterpret_cast<unsigned int *>(w + L.ticket), do_topk) != cudaSuccess)
+    return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 
@@ -689,8 +718,9 @@ qg_status launch_expert(MoeArgs a, cudaStream_t s) {
   const long long budget = dev.smem_optin - 4096;
   const long long ring_avail = budget - a.off_x - xbytes - 1024;
   if (ring_avail <= 0) return QG_EUNSUPPORTED;
-  const long long target = std::max<long long>(2048, std::min<long long>(6144, ring_avail / (3LL * NW)));
-  int gpc = static_cast<int>(std::max<long long>(1, target / (4LL * D::GB)));
+  // stages sized so that every warp gets 4 slots where possible
+  const long long target = std::max<long long>(2048, std::min<long long>(6144, ring_avail / (4LL * NW)));
+  int gpc = static_cast<int>(std::max<long long>(1, (target - 128) / (4LL * D::GB)));
   gpc = std::min(gpc, ngroups);
   a.seg_slot = static_cast<int>(((static_cast<long long>(gpc) * D::GB + 15) & ~15LL) + 32);
   a.stage_bytes = 4 * a.seg_slot;
@@ -702,7 +732,7 @@ qg_status launch_expert(MoeArgs a, cudaStream_t s) {
   const uint32_t smem = a.off_ring + static_cast<uint32_t>(NW * a.NS * a.stage_bytes) + 1024 + 64;
   auto kern = moe_expert_kernel<QT, TT, NW, DOWN>;
   if (!qg::set_smem_attr(reinterpret_cast<const void *>(kern), smem)) return QG_ECUDA;
-  kern<<<G, NW * 32, smem, s>>>(a);
+  if (qg::launch_pdl(kern, dim3(G), dim3(NW * 32), smem, s, a) != cudaSuccess) return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 
@@ -746,7 +776,8 @@ qg_status expert_checks(int type, int T, int k, int E, int H, int F, int n_slots
 
 qg_status swiglu_impl(int type, const void *w_gate, const void *w_up, int64_t stride, const int32_t *slots,
                       int n_slots, int E, const int32_t *ids, const float *xn, int T, int k, int H, int F,
-                      float *act, cudaStream_t s) {
+                      float *act, cudaStream_t s, const float *fused_logits = nullptr, int32_t *ids_out = nullptr,
+                      float *wts_out = nullptr) {
   if (!w_gate || !w_up || !ids || !xn || !act) return QG_EINVAL_PTR;
   const qg_status c = expert_checks(type, T, k, E, H, F, n_slots, stride);
   if (c != QG_OK) return c;
@@ -773,6 +804,12 @@ qg_status swiglu_impl(int type, const void *w_gate, const void *w_up, int64_t st
   a.F = F;
   a.K = H;
   a.R = F;
+  if (fused_logits) {
+    a.fuse_topk = 1;
+    a.logits = fused_logits;
+    a.ids_out = ids_out;
+    a.wts_out = wts_out;
+  }
   return launch_expert_type<false>(type, a, s);
 }
 
@@ -865,9 +902,13 @@ qg_status moe_layer(int type, const float *xn, const float *wr, const void *w_ga
   const qg_status c = expert_checks(type, T, k, E, H, F, n_slots, expert_stride);
   if (c != QG_OK) return c;
   if (ws_bytes < ws_layout(T, k, E, H).total) return QG_EWORKSPACE;
-  qg_status r = route_impl(xn, wr, T, H, E, k, ids, weights, nullptr, ws, ws_bytes, s);
+  // router logits into the workspace; the gate/up kernel ranks them (every CTA needs the
+  // picks for its plan anyway) and stores ids and weights for the combine
+  qg_status r = route_impl(xn, wr, T, H, E, k, ids, weights, nullptr, ws, ws_bytes, s, 0);
   if (r != QG_OK) return r;
-  r = swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, s);
+  const float *logits = reinterpret_cast<const float *>(static_cast<uint8_t *>(ws) + ws_layout(T, k, E, H).logits);
+  r = swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, s, logits, ids,
+                  weights);
   if (r != QG_OK) return r;
   return combine_impl(type, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout, 1, ws,
                       ws_bytes, s);

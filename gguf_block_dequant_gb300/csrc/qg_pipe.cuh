@@ -30,7 +30,7 @@ QG_DEVICE void load_x(uint8_t *dst, const CUtensorMap *map, int T, int N, int c,
 // Bytes to bulk-copy for [src, src + n) where src may be unaligned: the copy starts at the
 // 16-byte boundary below src (dst receives src at dst + (src & 15)); bytes past the
 // tensor's last 16-byte boundary `mend` are written here with plain loads instead.
-QG_DEVICE uint32_t stage_copy(uint8_t *dst, uintptr_t src, uint32_t n, uintptr_t mend, uint64_t *, bool) {
+QG_DEVICE uint32_t stage_copy(uint8_t *dst, uintptr_t src, uint32_t n, uintptr_t mend) {
   const uintptr_t al = src & ~static_cast<uintptr_t>(15);
   const uintptr_t want = (src + n + 15) & ~static_cast<uintptr_t>(15);
   if (want <= mend) return static_cast<uint32_t>(want - al);  // the usual case
@@ -39,6 +39,19 @@ QG_DEVICE uint32_t stage_copy(uint8_t *dst, uintptr_t src, uint32_t n, uintptr_t
   return nb;
 }
 
+// One bulk copy per active lane (each lane's own segment), all on one mbarrier: the byte
+// count of every segment is added to the barrier's transaction count before any copy starts.
+QG_DEVICE void warp_bulk_copies(uint8_t *dst, uintptr_t src, uint32_t n, uintptr_t mend, uint64_t *bar, int lane) {
+  uint32_t nb = 0;
+  if (n) nb = stage_copy(dst, src, n, mend);
+  const uint32_t tx = __reduce_add_sync(0xFFFFFFFFu, nb);
+  if (lane == 0) mbar_arrive_expect_tx(bar, tx);
+  __syncwarp();
+  if (nb) {
+    fence_proxy_async_smem();  // the slot's previous bytes were read through the generic proxy
+    bulk_g2s(dst, reinterpret_cast<const void *>(src & ~static_cast<uintptr_t>(15)), nb, bar);
+  }
+}
 
 // One-token inner loop over the groups of a stage: 4 rows (shared-memory unit addresses
 // wrow[r], already offset by the lane's unit) against the activation chunk whose first
