@@ -536,7 +536,7 @@ def run_moe(torch, qg, stream, hbm, layers=8, reps=50, warmup=3):
     pools = [base] + [base.clone() for _ in range(layers - 1)]
     wr = [torch.from_numpy(gs.router_weights(E, H, seed=l)).to(dev) for l in range(layers)]
     res = {}
-    for T in (1, 8):
+    for T in (1, 8, 512):
         xn = [torch.from_numpy(gs.activations(T, H, seed=l, stream=40)).to(dev) for l in range(layers)]
         x = torch.from_numpy(gs.activations(T, H, seed=0, stream=41)).to(dev)
         ids = torch.zeros((layers, T, k), dtype=torch.int32, device=dev)
@@ -550,8 +550,9 @@ def run_moe(torch, qg, stream, hbm, layers=8, reps=50, warmup=3):
                 qg.moe_layer(gs.Q8_0, xn[l], wr[l], p[go:], p[uo:], p[do:], stride, None, E, T, H, F, E, k,
                              ids[l], wts[l], act, x, ws)
         g = capture(torch, calls, stream)
-        el = time_graph(torch, g, stream, reps, warmup)
-        n = reps * layers
+        r = max(3, reps // 10) if T > 16 else reps
+        el = time_graph(torch, g, stream, r, warmup)
+        n = r * layers
         us = el / n * 1e6
         uniq = [len(np.unique(ids[l].cpu().numpy())) for l in range(layers)]
         U = float(np.mean(uniq))
@@ -560,7 +561,8 @@ def run_moe(torch, qg, stream, hbm, layers=8, reps=50, warmup=3):
         res[f"T{T}"] = {"us_per_layer": round(us, 2), "unique_experts": round(U, 2),
                         "bytes_per_layer": int(nbytes), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
                         "roofline_us": round(roof_us, 2), "frac_of_roofline": round(roof_us / us, 4),
-                        "launches_per_layer": 3, "tokens_per_s": round(T / (us * 1e-6), 1)}
+                        "launches_per_layer": 3 if T <= 16 else 8, "tokens_per_s": round(T / (us * 1e-6), 1),
+                        "path": "CUDA cores, grouped per expert" if T <= 16 else "tcgen05 grouped per expert (bf16)"}
         del g
         if qg.device_status() != 0:
             raise RuntimeError("device status set in the MoE benchmark")

@@ -93,7 +93,7 @@ qg_status qg_device_status(uint32_t *status_out, int clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return QG_ECUDA;
   const unsigned int a = qg::read_status_gemv(clear != 0);
   const unsigned int b = qg::read_status_moe(clear != 0);
-  const unsigned int c = qg::read_status_gemm(clear != 0);
+  const unsigned int c = qg::read_status_gemm(clear != 0) | qg::read_status_moetc(clear != 0);
   if (a == 0xFFFFFFFFu || b == 0xFFFFFFFFu || c == 0xFFFFFFFFu) return QG_ECUDA;
   *status_out = a | b | c;
   return QG_OK;

@@ -35,6 +35,7 @@
 #include "qg_common.cuh"
 #include "qg_host.h"
 #include "qg_pipe.cuh"
+#include "qg_tc.cuh"
 
 __device__ unsigned int g_qg_status_gemm;
 
@@ -62,93 +63,8 @@ constexpr uint32_t SMEM_BYTES = OFF_PARTS + MAX_PARTS * 4 + 1024;  // + alignmen
 constexpr uint32_t TMEM_COLS = 256;
 
 QG_DEVICE void gemm_status(unsigned int bits) { atomicOr(&g_qg_status_gemm, bits); }
-
-// ---- tcgen05 wrappers --------------------------------------------------------------------
-QG_DEVICE void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-               "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-QG_DEVICE void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-QG_DEVICE void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-QG_DEVICE void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-
-QG_DEVICE void tc_mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-      : "memory");
-}
-// arrives once on `bar` when every MMA this thread issued before it has completed
-QG_DEVICE void tc_commit(uint64_t *bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-// 32 consecutive f32 columns of this thread's TMEM lane
-QG_DEVICE void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Shared-memory matrix descriptor of a K-major operand tile in the 128-byte swizzled
-// layout: rows of 128 bytes, 8-row (1024-byte) swizzle atoms stacked along M/N.
-//   bits  0-13  start address >> 4        bits 16-29  leading byte offset >> 4 (unused here)
-//   bits 32-45  stride byte offset >> 4 (1024: next 8-row group)
-//   bits 46-47  descriptor version 1      bits 61-63  layout: 2 = 128-byte swizzle
-QG_DEVICE uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>(1u) << 16;
-  d |= static_cast<uint64_t>((1024u >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;
-  d |= static_cast<uint64_t>(2u) << 61;
-  return d;
-}
-
-// Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
-  return (1u << 4)                                 // D format f32
-         | (1u << 7)                               // A format bf16
-         | (1u << 10)                              // B format bf16
-         | (static_cast<uint32_t>(n >> 3) << 17)   // N / 8
-         | (static_cast<uint32_t>(m >> 4) << 24);  // M / 16
-}
-
-// ---- abort-aware bounded waits -------------------------------------------------------------
-QG_DEVICE bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
-  if (mbar_try_wait_sleep(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (true) {
-    if (mbar_try_wait_sleep(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_ns() - t0 > QG_WAIT_NS) break;
-  }
-  *abort_flag = 1;
-  gemm_status(QG_STATUS_BIT_TIMEOUT);
-  return false;
-}
-
-// short bounded wait used only while shutting down
-QG_DEVICE void cleanup_wait(uint64_t *bar, uint32_t parity) {
-  for (uint32_t i = 0; i < (1u << 16); ++i)
-    if (mbar_try_wait(bar, parity)) return;
+QG_DEVICE bool wait_or_abort_g(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+  return wait_or_abort(bar, parity, abort_flag, &g_qg_status_gemm);
 }
 
 struct GemmArgs {
@@ -165,50 +81,6 @@ QG_DEVICE long long range_start(long long b, long long total, int G) { return b 
 // the CTA whose range holds position p
 QG_DEVICE int range_owner(long long p, long long total, int G) {
   return static_cast<int>(((p + 1) * G + total - 1) / total - 1);
-}
-
-// Decode 16 Q8_0 weights (half hb & 1 of block hb >> 1 of the 64-k stage `sub`) of one row
-// from the raw stage into the A slot.  raw_row: shared address of the row's 272 raw bytes;
-// a_row: shared address of the row in the A slot (128 bytes, 16-byte chunks swizzled by
-// row & 7).  The 16 code bytes are fetched with two aligned 16-byte loads (eight lanes of
-// consecutive rows hit eight different bank groups: the raw row pitch is 17 chunks).
-QG_DEVICE void convert_half(uint32_t raw_row, int sub, int hb, uint32_t a_row, int row) {
-  const uint32_t blk = raw_row + 68u * static_cast<uint32_t>(sub) + 34u * static_cast<uint32_t>(hb >> 1);
-  uint32_t d16;
-  QG_LDS16(blk, 0, d16);
-  const float d = h2f(d16);
-  const uint32_t o = blk + 2u + 16u * static_cast<uint32_t>(hb & 1);
-  const uint32_t a16 = o & ~15u, off = o & 15u;
-  const uint4 v0 = lds_v4(a16), v1 = lds_v4(a16 + 16u);
-  const uint64_t q0 = (static_cast<uint64_t>(v0.y) << 32) | v0.x, q1 = (static_cast<uint64_t>(v0.w) << 32) | v0.z;
-  const uint64_t q2 = (static_cast<uint64_t>(v1.y) << 32) | v1.x, q3 = (static_cast<uint64_t>(v1.w) << 32) | v1.z;
-  const bool hi8 = off >= 8u;
-  const uint32_t sh = (off & 7u) * 8u;
-  const uint64_t l0 = hi8 ? q1 : q0, l1 = hi8 ? q2 : q1, l2 = hi8 ? q3 : q2;
-  const uint64_t lo = sh ? (l0 >> sh) | (l1 << (64u - sh)) : l0;
-  const uint64_t hi = sh ? (l1 >> sh) | (l2 << (64u - sh)) : l1;
-  const uint32_t cw[4] = {static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32), static_cast<uint32_t>(hi),
-                          static_cast<uint32_t>(hi >> 32)};
-  const f2 d2 = mk2(d, d);
-  const f2 bias = mk2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {  // two 16-byte chunks of 8 weights
-    uint32_t outw[4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t word = cw[2 * c + h] ^ 0x80808080u;
-      const f2 w01 = mul2(add2(mk2(magic_byte(word, 0), magic_byte(word, 1)), bias), d2);
-      const f2 w23 = mul2(add2(mk2(magic_byte(word, 2), magic_byte(word, 3)), bias), d2);
-      const __nv_bfloat162 b01 = __floats2bfloat162_rn(w01.x, w01.y);
-      const __nv_bfloat162 b23 = __floats2bfloat162_rn(w23.x, w23.y);
-      outw[2 * h] = *reinterpret_cast<const uint32_t *>(&b01);
-      outw[2 * h + 1] = *reinterpret_cast<const uint32_t *>(&b23);
-    }
-    const uint32_t chunk = static_cast<uint32_t>((2 * hb + c) ^ (row & 7));
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a_row + chunk * 16u), "r"(outw[0]), "r"(outw[1]),
-                 "r"(outw[2]), "r"(outw[3])
-                 : "memory");
-  }
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -269,7 +141,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int mt = tile / a.n_tt, tt = tile - mt * a.n_tt;
         for (int ks = k0; ks < k1 && ok; ++ks, ++rit) {
           const int r = static_cast<int>(rit % NRAW);
-          if (!wait_or_abort(&rempty[r], static_cast<uint32_t>(((rit / NRAW) & 1) ^ 1), abort_flag)) {
+          if (!wait_or_abort_g(&rempty[r], static_cast<uint32_t>(((rit / NRAW) & 1) ^ 1), abort_flag)) {
             ok = false;
             break;
           }
@@ -277,7 +149,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tma_load_2d(smem + OFF_RAW + r * RAW_BYTES, &wmap, ks * (RK / 32) * 17, mt * BM, &rfull[r]);
           for (int sub = 0; sub < RK / BK; ++sub, ++it) {
             const int s = static_cast<int>(it % NSTAGE);
-            if (!wait_or_abort(&empty[s], static_cast<uint32_t>(((it / NSTAGE) & 1) ^ 1), abort_flag)) {
+            if (!wait_or_abort_g(&empty[s], static_cast<uint32_t>(((it / NSTAGE) & 1) ^ 1), abort_flag)) {
               ok = false;
               break;
             }
@@ -307,7 +179,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int tile = static_cast<int>(pos / a.KS);
         const int k0 = static_cast<int>(pos - static_cast<long long>(tile) * a.KS);
         const int k1 = static_cast<int>(k0 + (end - pos) < a.KS ? k0 + (end - pos) : a.KS);
-        if (!wait_or_abort(acc_empty, static_cast<uint32_t>((si & 1) ^ 1), abort_flag)) {
+        if (!wait_or_abort_g(acc_empty, static_cast<uint32_t>((si & 1) ^ 1), abort_flag)) {
           ok = false;
           break;
         }
@@ -315,7 +187,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int ks = k0; ks < k1 && ok; ++ks) {
           for (int sub = 0; sub < RK / BK; ++sub, ++it) {
             const int s = static_cast<int>(it % NSTAGE);
-            if (!wait_or_abort(&full[s], static_cast<uint32_t>((it / NSTAGE) & 1), abort_flag)) {
+            if (!wait_or_abort_g(&full[s], static_cast<uint32_t>((it / NSTAGE) & 1), abort_flag)) {
               ok = false;
               break;
             }
@@ -352,13 +224,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int mt = tile / a.n_tt, tt = tile - mt * a.n_tt;
       for (int ks = k0; ks < k1 && ok; ++ks, ++rit) {
         const int r = static_cast<int>(rit % NRAW);
-        if (!wait_or_abort(&rfull[r], static_cast<uint32_t>((rit / NRAW) & 1), abort_flag)) {
+        if (!wait_or_abort_g(&rfull[r], static_cast<uint32_t>((rit / NRAW) & 1), abort_flag)) {
           ok = false;
           break;
         }
         for (int sub = 0; sub < RK / BK; ++sub, ++it) {
           const int s = static_cast<int>(it % NSTAGE);
-          if (!wait_or_abort(&empty[s], static_cast<uint32_t>(((it / NSTAGE) & 1) ^ 1), abort_flag)) {
+          if (!wait_or_abort_g(&empty[s], static_cast<uint32_t>(((it / NSTAGE) & 1) ^ 1), abort_flag)) {
             ok = false;
             break;
           }
@@ -373,7 +245,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       if (!ok) break;
       // ---- epilogue of this segment
-      if (!wait_or_abort(acc_full, static_cast<uint32_t>(si & 1), abort_flag)) {
+      if (!wait_or_abort_g(acc_full, static_cast<uint32_t>(si & 1), abort_flag)) {
         ok = false;
         break;
       }

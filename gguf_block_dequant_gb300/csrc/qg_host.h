@@ -47,7 +47,18 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 qg_status gemv_dispatch(int type, const void *w, const float *x, float *y, int64_t M, int64_t N, int T,
                         cudaStream_t s);
 
+// grouped tensor-core MoE expert steps for more than 16 tokens (qg_moe_tc.cu)
+bool moe_tc_supported(int type, int H, int F, int E);
+size_t moe_tc_workspace(int T, int k, int E, int H, int F);
+qg_status moe_swiglu_tc(const void *w_gate, const void *w_up, int64_t stride, const int32_t *slots, int n_slots,
+                        int E, const int32_t *ids, const float *xn, int T, int k, int H, int F, float *act, void *ws,
+                        cudaStream_t s);
+qg_status moe_combine_tc(const void *w_down, int64_t stride, const int32_t *slots, int n_slots, int E,
+                         const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
+                         float *x_inout, int add_residual, float *dn, void *ws, cudaStream_t s);
+
 unsigned int read_status_gemv(bool clear);
+unsigned int read_status_moetc(bool clear);
 unsigned int read_status_moe(bool clear);
 unsigned int read_status_gemm(bool clear);
 

@@ -184,6 +184,7 @@ struct MoeArgs {
   int nblk;          // row blocks per unit
   int KC, nchunks, NS, stage_bytes, seg_slot;
   int xrow_bytes;    // shared-memory bytes per token slot (whole groups of SG elements)
+  int gseg;          // whole-row stages of the gate/up kernel: offset of the up rows in a slot
   int add_residual;
   // gate/up kernel inside moe_layer: take the top-k picks from the router logits here
   // (every CTA ranks the logits itself; CTA 0 also stores ids and weights)
@@ -333,11 +334,12 @@ QG_DEVICE int build_plan(const MoeArgs &a, int TT, const PlanSmem &p) {
   return p.s_ustart[a.E];
 }
 
-// Row r of row block p of a unit: (tensor base, mend, row index) -- gate/up blocks are
-// {gate 2p, gate 2p+1, up 2p, up 2p+1}, down blocks are rows 4p .. 4p+3.
-template <bool DOWN>
-QG_DEVICE int block_row(const MoeArgs &a, int p, int r) {
-  return DOWN ? 4 * p + r : 2 * p + (r & 1);
+// Row r of row block p of a unit, for blocks of RR rows: a gate/up block is RR/2 gate rows
+// then the same RR/2 up rows ({gate p, up p} for RR = 2, {gate 2p, gate 2p+1, up 2p,
+// up 2p+1} for RR = 4); a down block is rows RR p .. RR p + RR - 1.
+template <bool DOWN, int RR>
+QG_DEVICE int block_row(int p, int r) {
+  return DOWN ? RR * p + r : (RR / 2) * p + (r % (RR / 2));
 }
 
 QG_DEVICE float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
@@ -354,9 +356,17 @@ QG_DEVICE void copy_x_row(uint8_t *xs, int slot, int xrow_bytes, const float *sr
   }
 }
 
+// rows per block: 2 for one token (so that whole-row stages stay large copies with 16
+// warps), 4 when several tokens share every decoded weight
+template <int TT>
+__host__ __device__ constexpr int moe_rows() {
+  return TT == 1 ? 2 : 4;
+}
+
 template <int QT, int TT, int NW, bool DOWN>
 __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a) {
   using D = Dec<QT>;
+  constexpr int RR = moe_rows<TT>(), HALF = RR / 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *wbar = reinterpret_cast<uint64_t *>(smem);  // [NW][kMaxNS]
@@ -403,24 +413,43 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
   uint8_t *wring = ring + warp * a.NS * a.stage_bytes;
   const uint32_t wring_s = smem_u32(wring);
 
+  // Stage of one item: whole rows (seg_slot == 0; one copy of the block's down rows, or one
+  // copy of its gate rows and one of its up rows) or one copy per row segment.
+  const bool whole = a.seg_slot == 0;
   auto issue = [&](int item, int s) {
     const int i = item / a.nchunks, c = item - i * a.nchunks;
     const long long rb = rbA + warp + static_cast<long long>(i) * NW;
     const int u = static_cast<int>(rb / a.nblk), p = static_cast<int>(rb - static_cast<long long>(u) * a.nblk);
     uint8_t *st = wring + s * a.stage_bytes;
+    const uintptr_t slot_off = static_cast<uintptr_t>(pl.u_slot[u]) * static_cast<uintptr_t>(a.stride);
     uintptr_t src = 0;
     uint32_t n = 0;
-    uint8_t *dst = st + lane * a.seg_slot;
+    uint8_t *dst = st;
     uintptr_t mend = 0;
-    if (lane < 4) {
-      const int row = block_row<DOWN>(a, p, lane);
+    if (whole) {
+      if (DOWN ? lane == 0 : lane < 2) {
+        const int r0 = DOWN ? RR * p : HALF * p;
+        const int nr = min(DOWN ? RR : HALF, a.R - r0);
+        const bool second = !DOWN && lane == 1;
+        if (nr > 0) {
+          n = static_cast<uint32_t>(nr) * static_cast<uint32_t>(a.row_bytes);
+          src = reinterpret_cast<uintptr_t>(second ? a.wb : a.wa) + slot_off +
+                static_cast<uintptr_t>(r0) * static_cast<uintptr_t>(a.row_bytes);
+          mend = second ? a.mend_b : a.mend_a;
+          dst = st + (second ? a.gseg : 0);
+        }
+      }
+    } else if (lane < RR) {
+      const int row = block_row<DOWN, RR>(p, lane);
       if (row < a.R) {
         const int kel = min(a.K - c * a.KC, a.KC);
         n = static_cast<uint32_t>(kel / D::QK) * D::BB;
-        const uint8_t *base = (DOWN || lane < 2) ? a.wa : a.wb;
-        mend = (DOWN || lane < 2) ? a.mend_a : a.mend_b;
-        src = reinterpret_cast<uintptr_t>(base) + static_cast<uintptr_t>(pl.u_slot[u]) * a.stride +
-              static_cast<uintptr_t>(row) * a.row_bytes + static_cast<uintptr_t>(c) * chunk_bytes;
+        const bool second = !DOWN && lane >= HALF;
+        src = reinterpret_cast<uintptr_t>(second ? a.wb : a.wa) + slot_off +
+              static_cast<uintptr_t>(row) * static_cast<uintptr_t>(a.row_bytes) +
+              static_cast<uintptr_t>(c) * static_cast<uintptr_t>(chunk_bytes);
+        mend = second ? a.mend_b : a.mend_a;
+        dst = st + lane * a.seg_slot;
       }
     }
     warp_bulk_copies(dst, src, n, mend, &wbar[warp * kMaxNS + s], lane);
@@ -454,8 +483,8 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
   const uint32_t xs_s = smem_u32(xs);
 
   bool ok = true;
-  float acc1[4];
-  f2 acc2[4][TT];
+  float acc1[RR];
+  f2 acc2[RR][TT];
   int consumed = 0;
   for (int item = 0; item < n_items; ++item) {
     if (issued < n_items) {
@@ -468,7 +497,7 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
     const int ucnt = pl.u_cnt[u];
     if (c == 0) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < RR; ++r) {
         acc1[r] = 0.f;
 #pragma unroll
         for (int t = 0; t < TT; ++t) acc2[r][t] = mk2(0.f, 0.f);
@@ -480,16 +509,27 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
       const int kel = min(a.K - c * a.KC, a.KC);
       const int gcount = (kel + D::SG - 1) / D::SG;
       const uint32_t st = wring_s + static_cast<uint32_t>(cs * a.stage_bytes);
-      uint32_t wrow[4];
+      uint32_t wrow[RR];
       {
+        // low 32 bits of the global addresses suffice: only their remainder mod 16 matters
         const uint32_t srow = static_cast<uint32_t>(pl.u_slot[u]) * static_cast<uint32_t>(a.stride);
         const uint32_t cb = static_cast<uint32_t>(c) * static_cast<uint32_t>(chunk_bytes);
+        const uint32_t rbytes = static_cast<uint32_t>(a.row_bytes);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int row = block_row<DOWN>(a, p, r);
-          const uint32_t base = static_cast<uint32_t>(reinterpret_cast<uintptr_t>((DOWN || r < 2) ? a.wa : a.wb));
-          const uint32_t addr = base + srow + static_cast<uint32_t>(row) * static_cast<uint32_t>(a.row_bytes) + cb;
-          wrow[r] = st + static_cast<uint32_t>(r * a.seg_slot) + (addr & 15u) + wo;
+        for (int r = 0; r < RR; ++r) {
+          const bool second = !DOWN && r >= HALF;
+          const int row = block_row<DOWN, RR>(p, r);
+          const uint32_t base = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(second ? a.wb : a.wa));
+          if (whole) {
+            // rows of one tensor are contiguous in the slot from the copy's first row
+            const int r0 = DOWN ? RR * p : HALF * p;
+            const uint32_t first = base + srow + static_cast<uint32_t>(r0) * rbytes;
+            wrow[r] = st + (second ? static_cast<uint32_t>(a.gseg) : 0u) + (first & 15u) +
+                      static_cast<uint32_t>(row - r0) * rbytes + wo;
+          } else {
+            const uint32_t addr = base + srow + static_cast<uint32_t>(row) * rbytes + cb;
+            wrow[r] = st + static_cast<uint32_t>(r * a.seg_slot) + (addr & 15u) + wo;
+          }
         }
       }
       // shared-memory offsets of the unit's token rows
@@ -510,27 +550,27 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
 #pragma unroll
           for (int ch = 0; ch < D::NCH; ++ch) xc[ch] = lds_f4(xt + xo[ch]);
           const float aux = D::xaux(xc);
-          typename D::U w[4];
+          typename D::U w[RR];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) w[r] = D::load(wrow[r] + goff, lane);
+          for (int r = 0; r < RR; ++r) w[r] = D::load(wrow[r] + goff, lane);
 #pragma unroll
-          for (int r = 0; r < 4; ++r) acc1[r] += D::dot1(w[r], xc, aux);
+          for (int r = 0; r < RR; ++r) acc1[r] += D::dot1(w[r], xc, aux);
         } else {
-          typename D::U w[4];
+          typename D::U w[RR];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) w[r] = D::load(wrow[r] + goff, lane);
+          for (int r = 0; r < RR; ++r) w[r] = D::load(wrow[r] + goff, lane);
 #pragma unroll
           for (int ch = 0; ch < D::NCH; ++ch) {
-            f2 w01[4], w23[4];
+            f2 w01[RR], w23[RR];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) D::weights(w[r], ch, w01[r], w23[r]);
+            for (int r = 0; r < RR; ++r) D::weights(w[r], ch, w01[r], w23[r]);
 #pragma unroll
             for (int t = 0; t < TT; ++t) {
               if (t < ucnt) {
                 const float4 xv = lds_f4(xg + toff[t] + xo[ch]);
                 const f2 x01 = mk2(xv.x, xv.y), x23 = mk2(xv.z, xv.w);
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
+                for (int r = 0; r < RR; ++r) {
                   acc2[r][t] = fma2(w01[r], x01, acc2[r][t]);
                   acc2[r][t] = fma2(w23[r], x23, acc2[r][t]);
                 }
@@ -544,8 +584,8 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
     ++consumed;
 
     if (c == a.nchunks - 1) {
-      // the unit's 4 x TT row sums, reduce-scattered over the warp
-      constexpr int NV = 4 * TT;
+      // the unit's RR x TT row sums, reduce-scattered over the warp
+      constexpr int NV = RR * TT;
       constexpr int NH = NV == 64 ? 2 : 1;
       float v[NV];
       if constexpr (!DOWN) {
@@ -553,45 +593,43 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
 #pragma unroll
         for (int t = 0; t < TT; ++t)
 #pragma unroll
-          for (int i = 0; i < 2; ++i)
+          for (int i = 0; i < HALF; ++i)
 #pragma unroll
             for (int gu = 0; gu < 2; ++gu) {
-              const int r = 2 * gu + i;
-              v[(t * 2 + i) * 2 + gu] = TT == 1 ? acc1[r] : acc2[r][t].x + acc2[r][t].y;
+              const int r = HALF * gu + i;
+              v[(t * HALF + i) * 2 + gu] = TT == 1 ? acc1[r] : acc2[r][t].x + acc2[r][t].y;
             }
       } else {
 #pragma unroll
         for (int t = 0; t < TT; ++t)
 #pragma unroll
-          for (int r = 0; r < 4; ++r) v[t * 4 + r] = TT == 1 ? acc1[r] : acc2[r][t].x + acc2[r][t].y;
+          for (int r = 0; r < RR; ++r) v[t * RR + r] = TT == 1 ? acc1[r] : acc2[r][t].x + acc2[r][t].y;
       }
       reduce_scatter<NV>(v, lane);
       const int i0 = rs_index<NV>(lane);
       const bool own = rs_owner<NV>(lane);
       if constexpr (!DOWN) {
         float g, uu;
-        int q;  // output index (t * 2 + i)
         if constexpr (NV == 64) {
           g = v[0];
           uu = v[1];
-          q = i0 >> 1;
         } else {
           g = v[0];
           uu = __shfl_down_sync(0xFFFFFFFFu, v[0], 1 << rs_shift<NV>());
-          q = i0 >> 1;
         }
-        const int t = q >> 1, i = 2 * p + (q & 1);
+        const int q = i0 >> 1;  // output index t * HALF + i
+        const int t = q / HALF, i = HALF * p + (q - (q / HALF) * HALF);
         const bool writer = (NV == 64 || (own && (i0 & 1) == 0));
         if (writer && ok && t < ucnt && i < a.F) {
           const int z = pl.s_pairs[pl.u_first[u] + t];
           a.out[static_cast<size_t>(z) * a.F + i] = silu_mul(g, uu);
         }
       } else {
-        const int h0 = 4 * p;
+        const int h0 = RR * p;
 #pragma unroll
         for (int hh = 0; hh < NH; ++hh) {
           const int idx = i0 + hh;
-          const int t = idx >> 2, r = idx & 3;
+          const int t = idx / RR, r = idx - (idx / RR) * RR;
           if (own && ok && t < ucnt && h0 + r < a.H) {
             const int z = pl.s_pairs[pl.u_first[u] + t];
             a.dn[static_cast<size_t>(z) * a.H + h0 + r] = v[hh];
@@ -609,7 +647,7 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
       const long long rb = rbA + warp + static_cast<long long>(i) * NW;
       const int u = static_cast<int>(rb / a.nblk), p = static_cast<int>(rb - static_cast<long long>(u) * a.nblk);
       const int ucnt = pl.u_cnt[u];
-      const int h0 = 4 * p;
+      const int h0 = RR * p;
       unsigned int last = 0;
       int tok = 0;
       if (lane < ucnt) {
@@ -624,7 +662,7 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
         lastm &= lastm - 1;
         const int tk = __shfl_sync(0xFFFFFFFFu, tok, src);
         const int h = h0 + lane;
-        if (lane < 4 && h < a.H) {
+        if (lane < RR && h < a.H) {
           float sum = 0.f;
           for (int j = 0; j < a.k; ++j) {
             const int zj = tk * a.k + j;
@@ -649,18 +687,21 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
 // ------------------------------------------------------------------------------------------
 
 struct WsLayout {
-  size_t logits, ticket, dn, cnt, total;
+  size_t logits, ticket, dn, cnt, tc, total;
 };
 
 inline size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-WsLayout ws_layout(int T, int k, int E, int H) {
+WsLayout ws_layout(int T, int k, int E, int H, int F = 0) {
   WsLayout w;
   w.logits = 0;
   w.ticket = up256(static_cast<size_t>(T) * E * 4);
   w.dn = w.ticket + up256(static_cast<size_t>((T + kRouterTB - 1) / kRouterTB) * 4);
   w.cnt = w.dn + up256(static_cast<size_t>(T) * k * H * 4);
-  w.total = w.cnt + up256(static_cast<size_t>(T) * ((H + 3) / 4) * 4);
+  w.tc = w.cnt + up256(static_cast<size_t>(T) * ((H + 1) / 2) * 4);  // counters for 2-row blocks
+  w.total = w.tc;
+  // grouped tensor-core path (more than 16 tokens): plan, grouped bf16 rows
+  if (T > 16 && F > 0) w.total += up256(qg::moe_tc_workspace(T, k, E, H, F));
   return w;
 }
 
@@ -694,13 +735,14 @@ template <int QT, int TT, bool DOWN>
 qg_status launch_expert(MoeArgs a, cudaStream_t s) {
   using D = Dec<QT>;
   constexpr int NW = (TT == 1) ? 16 : 8;
+  constexpr int RR = moe_rows<TT>(), HALF = RR / 2;
   const qg::DeviceInfo &dev = qg::device_info();
   if (!dev.ok) return QG_ECUDA;
   const int P = a.T * a.k;
   const int ngroups = (a.K + D::SG - 1) / D::SG;
   a.xrow_bytes = ngroups * D::SG * 4;
   a.row_bytes = static_cast<long long>(a.K / D::QK) * D::BB;
-  a.nblk = DOWN ? (a.H + 3) / 4 : (a.F + 1) / 2;
+  a.nblk = DOWN ? (a.H + RR - 1) / RR : (a.F + HALF - 1) / HALF;
   const int G = dev.sms;
   // token slots: all T tokens (gate/up); the units a CTA's row-block range can touch (down)
   int xslots = a.T;
@@ -718,16 +760,36 @@ qg_status launch_expert(MoeArgs a, cudaStream_t s) {
   const long long budget = dev.smem_optin - 4096;
   const long long ring_avail = budget - a.off_x - xbytes - 1024;
   if (ring_avail <= 0) return QG_EUNSUPPORTED;
-  // stages sized so that every warp gets 4 slots where possible
-  const long long target = std::max<long long>(2048, std::min<long long>(6144, ring_avail / (4LL * NW)));
-  int gpc = static_cast<int>(std::max<long long>(1, (target - 128) / (4LL * D::GB)));
-  gpc = std::min(gpc, ngroups);
-  a.seg_slot = static_cast<int>(((static_cast<long long>(gpc) * D::GB + 15) & ~15LL) + 32);
-  a.stage_bytes = 4 * a.seg_slot;
+  // Whole rows per stage when two such stages per warp fit: one copy of the block's down
+  // rows, or one of its gate rows and one of its up rows.  Otherwise one copy per row
+  // segment, segments of at least 2 KB (small bulk copies are capped by the copy engine's
+  // per-copy rate).
+  const long long half_bytes = ((static_cast<long long>(DOWN ? RR : HALF) * a.row_bytes + 15) & ~15LL) + 32;
+  const long long whole_stage = DOWN ? half_bytes : 2 * half_bytes;
+  if (2LL * NW * whole_stage <= ring_avail) {
+    a.seg_slot = 0;
+    a.gseg = DOWN ? 0 : static_cast<int>(half_bytes);
+    a.stage_bytes = static_cast<int>(whole_stage);
+    a.KC = ngroups * D::SG;
+    a.nchunks = 1;
+  } else {
+    const long long target = std::max<long long>(2048, std::min<long long>(16384, ring_avail / (2LL * NW)));
+    // the 2 KB floor first; without it when it leaves fewer than two slots per warp
+    for (int floor_groups : {std::min(ngroups, (2048 + D::GB - 1) / D::GB), 1}) {
+      int gmax = static_cast<int>(std::max<long long>(1, (target / RR - 32) / D::GB));
+      gmax = std::max(std::min(gmax, ngroups), floor_groups);
+      const int nch = (ngroups + gmax - 1) / gmax;
+      const int gpc = (ngroups + nch - 1) / nch;
+      a.seg_slot = static_cast<int>(((static_cast<long long>(gpc) * D::GB + 15) & ~15LL) + 32);
+      a.gseg = 0;
+      a.stage_bytes = RR * a.seg_slot;
+      a.KC = gpc * D::SG;
+      a.nchunks = nch;
+      if (ring_avail / (static_cast<long long>(NW) * a.stage_bytes) >= 2) break;
+    }
+  }
   a.NS = static_cast<int>(std::min<long long>(kMaxNS, ring_avail / (static_cast<long long>(NW) * a.stage_bytes)));
   if (a.NS < 2) return QG_EUNSUPPORTED;
-  a.KC = gpc * D::SG;
-  a.nchunks = (ngroups + gpc - 1) / gpc;
   a.off_ring = static_cast<uint32_t>(a.off_x + xbytes);
   const uint32_t smem = a.off_ring + static_cast<uint32_t>(NW * a.NS * a.stage_bytes) + 1024 + 64;
   auto kern = moe_expert_kernel<QT, TT, NW, DOWN>;
@@ -769,15 +831,16 @@ qg_status expert_checks(int type, int T, int k, int E, int H, int F, int n_slots
   const qg_status c = check_common(T, k, E, H, F);
   if (c != QG_OK) return c;
   if (H % qk || F % qk || n_slots < 1 || stride < 0) return QG_EINVAL_SHAPE;
-  if (T > 16) return QG_EUNSUPPORTED;  // decode path: up to 16 tokens per call
+  // more than 16 tokens: the grouped tensor-core path (Q8_0, rows in whole 256-element boxes)
+  if (T > 16 && (!qg::moe_tc_supported(type, H, F, E) || stride % 16)) return QG_EUNSUPPORTED;
   if (static_cast<long long>(stride) * n_slots > (1LL << 40)) return QG_EINVAL_SHAPE;
   return QG_OK;
 }
 
 qg_status swiglu_impl(int type, const void *w_gate, const void *w_up, int64_t stride, const int32_t *slots,
                       int n_slots, int E, const int32_t *ids, const float *xn, int T, int k, int H, int F,
-                      float *act, cudaStream_t s, const float *fused_logits = nullptr, int32_t *ids_out = nullptr,
-                      float *wts_out = nullptr) {
+                      float *act, void *ws, size_t ws_bytes, cudaStream_t s, const float *fused_logits = nullptr,
+                      int32_t *ids_out = nullptr, float *wts_out = nullptr) {
   if (!w_gate || !w_up || !ids || !xn || !act) return QG_EINVAL_PTR;
   const qg_status c = expert_checks(type, T, k, E, H, F, n_slots, stride);
   if (c != QG_OK) return c;
@@ -786,6 +849,14 @@ qg_status swiglu_impl(int type, const void *w_gate, const void *w_up, int64_t st
   qg_block_shape(type, &qk, &bb);
   const long long mat = static_cast<long long>(F) * (H / qk) * bb;
   if (n_slots > 1 && stride < mat) return QG_EINVAL_SHAPE;
+  if (T > 16) {
+    if (!ws) return QG_EINVAL_PTR;
+    if (!qg::aligned16(ws) || !qg::aligned16(w_gate) || !qg::aligned16(w_up)) return QG_EALIGN;
+    const WsLayout L = ws_layout(T, k, E, H, F);
+    if (ws_bytes < L.total) return QG_EWORKSPACE;
+    return qg::moe_swiglu_tc(w_gate, w_up, stride, slots, n_slots, E, ids, xn, T, k, H, F, act,
+                             static_cast<uint8_t *>(ws) + L.tc, s);
+  }
   MoeArgs a{};
   a.wa = static_cast<const uint8_t *>(w_gate);
   a.wb = static_cast<const uint8_t *>(w_up);
@@ -820,13 +891,18 @@ qg_status combine_impl(int type, const void *w_down, int64_t stride, const int32
   const qg_status c = expert_checks(type, T, k, E, H, F, n_slots, stride);
   if (c != QG_OK) return c;
   if (!qg::aligned16(act) || !qg::aligned16(ws)) return QG_EALIGN;
-  const WsLayout L = ws_layout(T, k, E, H);
+  const WsLayout L = ws_layout(T, k, E, H, F);
   if (ws_bytes < L.total) return QG_EWORKSPACE;
   int qk = 0, bb = 0;
   qg_block_shape(type, &qk, &bb);
   const long long mat = static_cast<long long>(H) * (F / qk) * bb;
   if (n_slots > 1 && stride < mat) return QG_EINVAL_SHAPE;
   uint8_t *w = static_cast<uint8_t *>(ws);
+  if (T > 16) {
+    if (!qg::aligned16(x_inout) || !qg::aligned16(w_down)) return QG_EALIGN;
+    return qg::moe_combine_tc(w_down, stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout,
+                              add_residual ? 1 : 0, reinterpret_cast<float *>(w + L.dn), w + L.tc, s);
+  }
   MoeArgs a{};
   a.wa = static_cast<const uint8_t *>(w_down);
   a.wb = a.wa;
@@ -870,7 +946,7 @@ extern "C" {
 
 size_t moe_workspace_size(int T, int k, int E, int H, int F) {
   if (check_common(T, k, E, H, F) != QG_OK) return 0;
-  return ws_layout(T, k, E, H).total;
+  return ws_layout(T, k, E, H, F).total;
 }
 
 qg_status moe_route_topk(const float *xn, const float *wr, int T, int H, int E, int k, int32_t *ids, float *weights,
@@ -881,8 +957,8 @@ qg_status moe_route_topk(const float *xn, const float *wr, int T, int H, int E, 
 
 qg_status moe_expert_swiglu(int type, const void *w_gate, const void *w_up, int64_t expert_stride,
                             const int32_t *slots, int n_slots, int E, const int32_t *ids, const float *xn, int T,
-                            int k, int H, int F, float *act, void *, size_t, qg_stream_t stream) {
-  return swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act,
+                            int k, int H, int F, float *act, void *ws, size_t ws_bytes, qg_stream_t stream) {
+  return swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -901,14 +977,24 @@ qg_status moe_layer(int type, const float *xn, const float *wr, const void *w_ga
   if (!xn || !wr || !w_gate || !w_up || !w_down || !ids || !weights || !act || !x_inout || !ws) return QG_EINVAL_PTR;
   const qg_status c = expert_checks(type, T, k, E, H, F, n_slots, expert_stride);
   if (c != QG_OK) return c;
-  if (ws_bytes < ws_layout(T, k, E, H).total) return QG_EWORKSPACE;
+  if (ws_bytes < ws_layout(T, k, E, H, F).total) return QG_EWORKSPACE;
+  qg_status r;
+  if (T > 16) {
+    // prefill-sized batch: router with top-k, then the grouped tensor-core expert steps
+    r = route_impl(xn, wr, T, H, E, k, ids, weights, nullptr, ws, ws_bytes, s, 1);
+    if (r != QG_OK) return r;
+    r = swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes, s);
+    if (r != QG_OK) return r;
+    return combine_impl(type, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout, 1,
+                        ws, ws_bytes, s);
+  }
   // router logits into the workspace; the gate/up kernel ranks them (every CTA needs the
   // picks for its plan anyway) and stores ids and weights for the combine
-  qg_status r = route_impl(xn, wr, T, H, E, k, ids, weights, nullptr, ws, ws_bytes, s, 0);
+  r = route_impl(xn, wr, T, H, E, k, ids, weights, nullptr, ws, ws_bytes, s, 0);
   if (r != QG_OK) return r;
   const float *logits = reinterpret_cast<const float *>(static_cast<uint8_t *>(ws) + ws_layout(T, k, E, H).logits);
-  r = swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, s, logits, ids,
-                  weights);
+  r = swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes, s,
+                  logits, ids, weights);
   if (r != QG_OK) return r;
   return combine_impl(type, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout, 1, ws,
                       ws_bytes, s);

@@ -18,6 +18,14 @@ QG_DEVICE void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, ui
       : "memory");
 }
 
+QG_DEVICE void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // T activation rows blocks [row0(t), row0(t) + xR) into the buffer at dst (1024-byte aligned),
 // with expect_tx on bar
 QG_DEVICE void load_x(uint8_t *dst, const CUtensorMap *map, int T, int N, int c, int xR, int box_rows,

@@ -264,8 +264,8 @@ def test_moe_shape_errors(qg):
     with pytest.raises(qg.QGError) as e:
         qg.moe_route_topk(f, f, 4, 64, 8, 2, i, f, None, d[:16])  # workspace too small
     assert e.value.status == qg.QG_EWORKSPACE
-    with pytest.raises(qg.QGError) as e:
-        qg.moe_expert_swiglu(gs.Q8_0, d, d, 0, None, 1, 8, i, f, 17, 2, 64, 32, f)  # T > 16 on this path
+    with pytest.raises(qg.QGError) as e:  # more than 16 tokens needs rows in whole 256-element boxes
+        qg.moe_expert_swiglu(gs.Q8_0, d, d, 0, None, 1, 8, i, f, 17, 2, 64, 32, f)
     assert e.value.status == qg.QG_EUNSUPPORTED
 
 
@@ -304,3 +304,125 @@ def test_moe_layer_qwen3_30b_a3b(qg, oracle_lib, a3b, T):
     check_route(oracle_lib, xn, wr, k, ids_h, wts_h, lg, what=f"layer T={T}")
     check_swiglu(oracle_lib, ex, ids_h, xn, k, act_h, what=f"layer T={T}")
     check_combine(oracle_lib, ex, ids_h, wts_h, act_h, x, k, outs[0], what=f"layer T={T}")
+
+
+# ---- more than 16 tokens: grouped tensor-core path (bf16 operands, f32 accumulation) ----------
+
+PREFILL_REL = 2e-3  # the prefill bar: |gpu - oracle| <= 2e-3 * sum|w x| + 1e-6
+
+
+class ExactExperts(Experts):
+    """Q8_0 expert records with d = 1.0 and codes in [-4, 4]: exact in bf16."""
+
+    def __init__(self, E, H, F, seed=0):
+        self.qtype, self.E, self.H, self.F, self.n_slots = gs.Q8_0, E, H, F, E
+        go, uo, do, stride = gs.moe_expert_record_layout(H, F, gs.Q8_0)
+        self.offs, self.stride = (go, uo, do), stride
+        rng = np.random.default_rng(seed)
+        blk = np.empty((E * stride // 34, 34), np.uint8)
+        blk[:, 0], blk[:, 1] = 0x00, 0x3C
+        blk[:, 2:] = rng.integers(-4, 5, size=(blk.shape[0], 32)).astype(np.int8).view(np.uint8)
+        self.host = blk.reshape(-1)
+        self.dev = to_dev(self.host, torch)
+
+
+def test_grouped_gate_up_exact_products(qg, oracle_lib):
+    """Integer weights and activations: every gate/up product and sum is exact, so act can
+    differ from the oracle only by the f32 evaluation of silu(g) * u."""
+    E, H, F, k, T = 8, 256, 256, 2, 40
+    ex = ExactExperts(E, H, F, seed=1)
+    ids = _rand_ids(T, k, E, seed=4)
+    xn = np.random.default_rng(5).integers(-2, 3, size=(T, H)).astype(np.float32)
+    gate, up, _ = ex.bases()
+    act = torch.full((T * k, F), float("nan"), dtype=torch.float32, device="cuda")
+    ws = _ws(qg, T, k, E, H, F)
+    qg.moe_expert_swiglu(gs.Q8_0, gate, up, ex.stride, None, E, E, to_dev(ids, torch), to_dev(xn, torch), T, k, H, F,
+                         act, ws)
+    torch.cuda.synchronize()
+    assert qg.device_status() == 0
+    g, u, ref, _, _ = oracle_lib.moe_gate_up(gs.Q8_0, ex.host[ex.offs[0]:], ex.host[ex.offs[1]:], ex.stride, None, ids,
+                                             xn, k, H, F)
+    assert np.array_equal(np.round(g), g) and np.array_equal(np.round(u), u)
+    got = act.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - ref) <= 1e-6 * np.abs(ref) + 1e-30), np.abs(got - ref).max()
+
+
+@pytest.mark.parametrize("T", [17, 100])
+def test_grouped_experts_slots_and_bad_id(qg, oracle_lib, T):
+    H, F, E, k = 512, 256, 12, 3
+    ex = Experts(gs.Q8_0, E, H, F, n_slots=15, seed=6)
+    slots = np.random.default_rng(2).permutation(15)[:E].astype(np.int32)
+    ids = _rand_ids(T, k, E, seed=T)
+    ids[T // 2, 1] = -3  # bad id: flagged, act row zero, left out of the combine
+    xn = gs.activations(T, H, seed=T, stream=51)
+    gate, up, down = ex.bases()
+    ws = _ws(qg, T, k, E, H, F)
+    act = torch.full((T * k, F), float("nan"), dtype=torch.float32, device="cuda")
+    sl = to_dev(slots, torch)
+    qg.moe_expert_swiglu(gs.Q8_0, gate, up, ex.stride, sl, ex.n_slots, E, to_dev(ids, torch), to_dev(xn, torch), T, k,
+                         H, F, act, ws)
+    torch.cuda.synchronize()
+    assert qg.device_status() & (1 << qg.QG_EDEVICE_ID)
+    act_h = act.cpu().numpy()
+    bad = (T // 2) * k + 1
+    assert (act_h[bad] == 0).all()
+    ids_ok = ids.copy()
+    ids_ok[T // 2, 1] = ids[T // 2, 0]
+    g, u, ref, bg, bu = oracle_lib.moe_gate_up(gs.Q8_0, ex.host[ex.offs[0]:], ex.host[ex.offs[1]:], ex.stride, slots,
+                                               ids_ok, xn, k, H, F, threads=8)
+    eg, eu = PREFILL_REL * bg + 1e-6, PREFILL_REL * bu + 1e-6
+    sig = 1.0 / (1.0 + np.exp(-g))
+    lim = np.abs(sig * (1 + g * (1 - sig)) * u) * eg + np.abs(g * sig) * eu + 1e-6
+    good = np.ones(T * k, bool)
+    good[bad] = False
+    assert (np.abs(act_h[good] - ref[good]) <= lim[good]).all()
+    wts = np.random.default_rng(T).random((T, k)).astype(np.float32)
+    x = gs.activations(T, H, seed=T, stream=52)
+    xd = to_dev(x, torch)
+    qg.moe_combine(gs.Q8_0, down, ex.stride, sl, ex.n_slots, E, to_dev(ids, torch), to_dev(wts, torch),
+                   to_dev(act_h, torch), T, k, H, F, xd, 1, ws)
+    torch.cuda.synchronize()
+    assert qg.device_status() & (1 << qg.QG_EDEVICE_ID)
+    wts_ok = wts.copy()
+    wts_ok[T // 2, 1] = 0.0
+    _, _, out_ref, bout = oracle_lib.moe_down_combine(gs.Q8_0, ex.host[ex.offs[2]:], ex.stride, slots, ids_ok, wts_ok,
+                                                      act_h, x, k, H, F, 1, threads=8)
+    assert_within_bound(xd.cpu().numpy(), out_ref, bout, rel=PREFILL_REL, what=f"grouped combine T={T}")
+
+
+@pytest.mark.parametrize("T", [64, 512])
+def test_moe_layer_prefill_grouped(qg, oracle_lib, a3b, T):
+    """The Qwen3-30B-A3B-shaped layer on a prefill batch: router and top-k as in decode, the
+    expert steps grouped per expert on the tensor cores."""
+    H, F, E, k = gs.MOE_H, gs.MOE_F, gs.MOE_E, gs.MOE_K
+    ex = a3b
+    wr = gs.router_weights(E, H, seed=0)
+    xn = gs.activations(T, H, seed=T, stream=61)
+    x = gs.activations(T, H, seed=T, stream=62)
+    gate, up, down = ex.bases()
+    ids = torch.zeros((T, k), dtype=torch.int32, device="cuda")
+    wts = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    act = torch.zeros((T * k, F), dtype=torch.float32, device="cuda")
+    ws = _ws(qg, T, k, E, H, F)
+    xd = to_dev(x, torch)
+    qg.moe_layer(gs.Q8_0, to_dev(xn, torch), to_dev(wr, torch), gate, up, down, ex.stride, None, E, T, H, F, E, k, ids,
+                 wts, act, xd, ws)
+    torch.cuda.synchronize()
+    assert qg.device_status() == 0
+    ids_h, wts_h, act_h = ids.cpu().numpy(), wts.cpu().numpy(), act.cpu().numpy()
+    i2, w2, lg = _route(qg, xn, wr, k)
+    assert np.array_equal(i2, ids_h) and np.array_equal(w2, wts_h)
+    check_route(oracle_lib, xn, wr, k, ids_h, wts_h, lg, what=f"prefill T={T}")
+    # sampled pairs for the gate/up stage (the oracle's full stage at T = 512 is slow)
+    rng = np.random.default_rng(T)
+    toks = np.unique(np.concatenate([[0, T - 1], rng.integers(0, T, 12)]))
+    g, u, ref, bg, bu = oracle_lib.moe_gate_up(gs.Q8_0, ex.host[ex.offs[0]:], ex.host[ex.offs[1]:], ex.stride, None,
+                                               ids_h[toks], xn[toks], k, H, F, threads=16)
+    eg, eu = PREFILL_REL * bg + 1e-6, PREFILL_REL * bu + 1e-6
+    sig = 1.0 / (1.0 + np.exp(-g))
+    lim = np.abs(sig * (1 + g * (1 - sig)) * u) * eg + np.abs(g * sig) * eu + 1e-6
+    rows = (toks[:, None] * k + np.arange(k)[None, :]).reshape(-1)
+    assert (np.abs(act_h[rows] - ref) <= lim).all(), "prefill act"
+    _, _, out_ref, bout = oracle_lib.moe_down_combine(gs.Q8_0, ex.host[ex.offs[2]:], ex.stride, None, ids_h[toks],
+                                                      wts_h[toks], act_h[rows], x[toks], k, H, F, 1, threads=16)
+    assert_within_bound(xd.cpu().numpy()[toks], out_ref, bout, rel=PREFILL_REL, what=f"prefill combine T={T}")
