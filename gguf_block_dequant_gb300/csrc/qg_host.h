@@ -53,6 +53,11 @@ size_t moe_tc_workspace(int T, int k, int E, int H, int F);
 qg_status moe_swiglu_tc(const void *w_gate, const void *w_up, int64_t stride, const int32_t *slots, int n_slots,
                         int E, const int32_t *ids, const float *xn, int T, int k, int H, int F, float *act, void *ws,
                         cudaStream_t s);
+// x[t] = (add_residual ? x[t] : 0) + sum_j w[t][j] dn[t k + j] in pick order, from dn rows in
+// memory (both MoE paths)
+qg_status moe_launch_combine(const float *dn, const float *weights, const int32_t *ids, const int32_t *slots,
+                             int n_slots, int E, int T, int k, int H, float *x_inout, int add_residual,
+                             cudaStream_t s);
 qg_status moe_combine_tc(const void *w_down, int64_t stride, const int32_t *slots, int n_slots, int E,
                          const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
                          float *x_inout, int add_residual, float *dn, void *ws, cudaStream_t s);

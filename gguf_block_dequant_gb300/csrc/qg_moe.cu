@@ -18,13 +18,14 @@
 // memory.  Each expert's weight bytes cross HBM once per call, for all of its tokens.
 //
 // Gate/up epilogue: act[z][i] = g_i / (1 + exp(-g_i)) * u_i written straight from the warp's
-// four sums.  Down epilogue: the warp writes its four dn values of each pair to the
-// workspace, then counts the pair in a per-(token, row-block) counter; the warp that
-// completes a token's k picks forms  x[t][h] = x[t][h] + sum_j w_j * dn_j[h]  in pick order
-// (deterministic) and resets the counter, so the workspace is zero again after every call.
+// sums.  Down epilogue: the warp writes the dn values of each pair to the workspace; a small
+// combine kernel then forms  x[t][h] = x[t][h] + sum_j w_j * dn_j[h]  in pick order
+// (deterministic), launched with programmatic dependent launch so that it starts as the down
+// kernel drains.
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "qg_decode.cuh"
 #include "qg_host.h"
@@ -176,7 +177,6 @@ struct MoeArgs {
   const float *xin;  // xn [T][H] (gate/up) or act [T*k][F] (down)
   float *out;        // act [T*k][F] (gate/up) or x_inout [T][H] (down)
   float *dn;         // [T*k][H] workspace (down)
-  unsigned int *cnt; // [T][nblk] workspace counters (down)
   int T, k, H, F;
   int K;             // dot length: H (gate/up) or F (down)
   int R;             // rows of one expert matrix: F (gate/up) or H (down)
@@ -186,6 +186,7 @@ struct MoeArgs {
   int xrow_bytes;    // shared-memory bytes per token slot (whole groups of SG elements)
   int gseg;          // whole-row stages of the gate/up kernel: offset of the up rows in a slot
   int add_residual;
+  int box_rows;      // one token: rows (of 32 floats) per activation tensor copy
   // gate/up kernel inside moe_layer: take the top-k picks from the router logits here
   // (every CTA ranks the logits itself; CTA 0 also stores ids and weights)
   int fuse_topk;
@@ -334,6 +335,44 @@ QG_DEVICE int build_plan(const MoeArgs &a, int TT, const PlanSmem &p) {
   return p.s_ustart[a.E];
 }
 
+// One token (every pick its own unit): each warp builds the identical plan in shared memory
+// by itself (the same values land at the same addresses from every warp), so no CTA barrier
+// is needed.  With fuse_topk the warp first ranks the router logits.  Returns the units.
+QG_DEVICE int warp_plan_one_token(const MoeArgs &a, const PlanSmem &p, int lane) {
+  const int P = a.k;  // one token: P = k <= 32
+  if (a.fuse_topk) {
+    topk_token(a.logits, a.E, a.k, lane, p.tk_ids, p.tk_w);
+    __syncwarp();
+    if (blockIdx.x == 0 && threadIdx.x < 32 && lane < P) {
+      a.ids_out[lane] = p.tk_ids[lane];
+      a.wts_out[lane] = p.tk_w[lane];
+    }
+  }
+  bool ok = false;
+  int e = -1, slot = -1;
+  if (lane < P) {
+    e = a.fuse_topk ? p.tk_ids[lane] : __ldg(a.ids + lane);
+    ok = e >= 0 && e < a.E;
+    if (ok) {
+      slot = a.slots ? __ldg(a.slots + e) : e;
+      ok = slot >= 0 && slot < a.n_slots;
+    }
+    p.s_id[lane] = ok ? e : -1;
+    if (!ok && blockIdx.x == 0 && threadIdx.x < 32) moe_status(QG_STATUS_BIT_ID);
+  }
+  const unsigned int mask = __ballot_sync(0xFFFFFFFFu, ok);
+  if (ok) {
+    const int rank = __popc(mask & ((1u << lane) - 1u));
+    p.s_pairs[rank] = lane;
+    p.u_slot[rank] = slot;
+    p.u_first[rank] = rank;
+    p.u_cnt[rank] = 1;
+  }
+  if (lane == 0) p.s_kv[0] = __popc(mask);
+  __syncwarp();
+  return __popc(mask);
+}
+
 // Row r of row block p of a unit, for blocks of RR rows: a gate/up block is RR/2 gate rows
 // then the same RR/2 up rows ({gate p, up p} for RR = 2, {gate 2p, gate 2p+1, up 2p,
 // up 2p+1} for RR = 4); a down block is rows RR p .. RR p + RR - 1.
@@ -364,12 +403,14 @@ __host__ __device__ constexpr int moe_rows() {
 }
 
 template <int QT, int TT, int NW, bool DOWN>
-__global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a) {
+__global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                const MoeArgs a) {
   using D = Dec<QT>;
   constexpr int RR = moe_rows<TT>(), HALF = RR / 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *wbar = reinterpret_cast<uint64_t *>(smem);  // [NW][kMaxNS]
+  uint64_t *xbar = wbar + NW * kMaxNS;                   // one token: activation rows by TMA
   const int P = a.T * a.k;
   const PlanSmem pl = plan_layout(smem + a.off_plan, P, a.T);
   uint8_t *xs = smem + a.off_x;
@@ -378,11 +419,17 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NW * kMaxNS; ++i) mbar_init(&wbar[i], 1);
+    mbar_init(xbar, 1);
     fence_mbar_init();
   }
+  __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
-  const int nunits = build_plan<NW>(a, TT, pl);
+  int nunits;
+  if constexpr (TT == 1)
+    nunits = warp_plan_one_token(a, pl, lane);
+  else
+    nunits = build_plan<NW>(a, TT, pl);
 
   // pairs with a bad id: their act row is zero (gate/up); tokens without any valid pick keep
   // (or clear) their residual (down)
@@ -390,10 +437,6 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
     if constexpr (!DOWN) {
       for (int i = threadIdx.x; i < P * a.F; i += NW * 32)
         if (pl.s_id[i / a.F] < 0) a.out[i] = 0.f;
-    } else {
-      if (!a.add_residual)
-        for (int i = threadIdx.x; i < a.T * a.H; i += NW * 32)
-          if (pl.s_kv[i / a.H] == 0) a.out[i] = 0.f;
     }
   }
 
@@ -459,19 +502,35 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
   for (; issued < a.NS - 1 && issued < n_items; ++issued) issue(issued, issued % a.NS);
 
   // activations of the tokens this CTA needs (the first weight stages are already in flight)
-  if constexpr (!DOWN) {
-    for (int t = 0; t < a.T; ++t)
-      copy_x_row(xs, t, a.xrow_bytes, a.xin + static_cast<size_t>(t) * a.K, a.K, threadIdx.x, NW * 32);
-  } else {
-    for (int u = uA; u <= uB; ++u)
-      for (int t = 0; t < pl.u_cnt[u]; ++t) {
-        const int z = pl.s_pairs[pl.u_first[u] + t];
-        copy_x_row(xs, (u - uA) * TT + t, a.xrow_bytes, a.xin + static_cast<size_t>(z) * a.K, a.K, threadIdx.x,
-                   NW * 32);
+  bool x_ok = true;
+  if constexpr (TT == 1) {
+    // one token: tensor copies with the 128-byte swizzle, waited for by each warp
+    const int R = a.K / 32;  // 32-float rows per activation row
+    if (threadIdx.x == 0) {
+      const int nslot = DOWN ? uB - uA + 1 : 1;
+      mbar_arrive_expect_tx(xbar, static_cast<uint32_t>(nslot * R) * 128u);
+      for (int sl = 0; sl < nslot; ++sl) {
+        const int row = DOWN ? pl.s_pairs[pl.u_first[uA + sl]] : 0;
+        for (int b = 0; b < R; b += a.box_rows)
+          tma_load_2d(xs + static_cast<size_t>(sl) * a.xrow_bytes + b * 128, &xmap, 0, row * R + b, xbar);
       }
+    }
+    x_ok = mbar_wait(xbar, 0);
+  } else {
+    if constexpr (!DOWN) {
+      for (int t = 0; t < a.T; ++t)
+        copy_x_row(xs, t, a.xrow_bytes, a.xin + static_cast<size_t>(t) * a.K, a.K, threadIdx.x, NW * 32);
+    } else {
+      for (int u = uA; u <= uB; ++u)
+        for (int t = 0; t < pl.u_cnt[u]; ++t) {
+          const int z = pl.s_pairs[pl.u_first[u] + t];
+          copy_x_row(xs, (u - uA) * TT + t, a.xrow_bytes, a.xin + static_cast<size_t>(z) * a.K, a.K, threadIdx.x,
+                     NW * 32);
+        }
+    }
+    cp_async_wait_all();
+    __syncthreads();
   }
-  cp_async_wait_all();
-  __syncthreads();
 
   if (n_items == 0) return;
 
@@ -482,7 +541,7 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
   const int gpc = a.KC / D::SG;
   const uint32_t xs_s = smem_u32(xs);
 
-  bool ok = true;
+  bool ok = x_ok;
   float acc1[RR];
   f2 acc2[RR][TT];
   int consumed = 0;
@@ -638,43 +697,6 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
       }
     }
   }
-  if constexpr (DOWN) {
-    // one fence for all of this warp's dn values, then each (token, row block) pick is
-    // counted; the pick that completes a token's valid picks forms that token's combine
-    __threadfence();
-    __syncwarp();
-    for (int i = 0; i < my_rbs && ok; ++i) {
-      const long long rb = rbA + warp + static_cast<long long>(i) * NW;
-      const int u = static_cast<int>(rb / a.nblk), p = static_cast<int>(rb - static_cast<long long>(u) * a.nblk);
-      const int ucnt = pl.u_cnt[u];
-      const int h0 = RR * p;
-      unsigned int last = 0;
-      int tok = 0;
-      if (lane < ucnt) {
-        tok = pl.s_pairs[pl.u_first[u] + lane] / a.k;
-        const unsigned int old = atomicAdd(&a.cnt[static_cast<size_t>(tok) * a.nblk + p], 1u);
-        last = (old + 1u == static_cast<unsigned int>(pl.s_kv[tok])) ? 1u : 0u;
-      }
-      unsigned int lastm = __ballot_sync(0xFFFFFFFFu, last != 0);
-      if (lastm) __threadfence();
-      while (lastm) {
-        const int src = __ffs(lastm) - 1;
-        lastm &= lastm - 1;
-        const int tk = __shfl_sync(0xFFFFFFFFu, tok, src);
-        const int h = h0 + lane;
-        if (lane < RR && h < a.H) {
-          float sum = 0.f;
-          for (int j = 0; j < a.k; ++j) {
-            const int zj = tk * a.k + j;
-            if (pl.s_id[zj] >= 0) sum = fmaf(__ldg(a.wts + zj), __ldcg(a.dn + static_cast<size_t>(zj) * a.H + h), sum);
-          }
-          float *o = a.out + static_cast<size_t>(tk) * a.H + h;
-          *o = a.add_residual ? *o + sum : sum;
-        }
-        if (lane == 0) a.cnt[static_cast<size_t>(tk) * a.nblk + p] = 0u;
-      }
-    }
-  }
   if (!ok) {
     if (lane == 0) moe_status(QG_STATUS_BIT_TIMEOUT);
     if (lane == 0)
@@ -687,7 +709,7 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const MoeArgs a)
 // ------------------------------------------------------------------------------------------
 
 struct WsLayout {
-  size_t logits, ticket, dn, cnt, tc, total;
+  size_t logits, ticket, dn, tc, total;
 };
 
 inline size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -697,8 +719,7 @@ WsLayout ws_layout(int T, int k, int E, int H, int F = 0) {
   w.logits = 0;
   w.ticket = up256(static_cast<size_t>(T) * E * 4);
   w.dn = w.ticket + up256(static_cast<size_t>((T + kRouterTB - 1) / kRouterTB) * 4);
-  w.cnt = w.dn + up256(static_cast<size_t>(T) * k * H * 4);
-  w.tc = w.cnt + up256(static_cast<size_t>(T) * ((H + 1) / 2) * 4);  // counters for 2-row blocks
+  w.tc = w.dn + up256(static_cast<size_t>(T) * k * H * 4);
   w.total = w.tc;
   // grouped tensor-core path (more than 16 tokens): plan, grouped bf16 rows
   if (T > 16 && F > 0) w.total += up256(qg::moe_tc_workspace(T, k, E, H, F));
@@ -753,7 +774,7 @@ qg_status launch_expert(MoeArgs a, cudaStream_t s) {
     const long long span = std::min<long long>(umax, (L - 1) / a.nblk + 2);
     xslots = static_cast<int>(span) * TT;
   }
-  const uint32_t hdr = 1024;
+  const uint32_t hdr = 1024;  // mbarriers: NW * kMaxNS + 1 of them
   a.off_plan = hdr;
   a.off_x = (a.off_plan + plan_bytes(P, a.T) + 1023) & ~1023u;
   const long long xbytes = static_cast<long long>(xslots) * a.xrow_bytes;
@@ -792,9 +813,22 @@ qg_status launch_expert(MoeArgs a, cudaStream_t s) {
   if (a.NS < 2) return QG_EUNSUPPORTED;
   a.off_ring = static_cast<uint32_t>(a.off_x + xbytes);
   const uint32_t smem = a.off_ring + static_cast<uint32_t>(NW * a.NS * a.stage_bytes) + 1024 + 64;
+  // one token: tensor map over the activation rows ([rows * K / 32][32] f32, 128-byte swizzle)
+  CUtensorMap xmap;
+  memset(&xmap, 0, sizeof(xmap));
+  if (TT == 1) {
+    const int R = a.K / 32;  // largest box height <= 256 dividing the rows of one activation row
+    a.box_rows = 1;
+    for (int d = std::min(R, 256); d >= 1; --d)
+      if (R % d == 0) {
+        a.box_rows = d;
+        break;
+      }
+    if (!qg::encode_x_map(&xmap, a.xin, DOWN ? P : a.T, a.K, a.box_rows)) return QG_ECUDA;
+  }
   auto kern = moe_expert_kernel<QT, TT, NW, DOWN>;
   if (!qg::set_smem_attr(reinterpret_cast<const void *>(kern), smem)) return QG_ECUDA;
-  if (qg::launch_pdl(kern, dim3(G), dim3(NW * 32), smem, s, a) != cudaSuccess) return QG_ECUDA;
+  if (qg::launch_pdl(kern, dim3(G), dim3(NW * 32), smem, s, xmap, a) != cudaSuccess) return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 
@@ -917,7 +951,6 @@ qg_status combine_impl(int type, const void *w_down, int64_t stride, const int32
   a.xin = act;
   a.out = x_inout;
   a.dn = reinterpret_cast<float *>(w + L.dn);
-  a.cnt = reinterpret_cast<unsigned int *>(w + L.cnt);
   a.T = T;
   a.k = k;
   a.H = H;
@@ -925,7 +958,10 @@ qg_status combine_impl(int type, const void *w_down, int64_t stride, const int32
   a.K = F;
   a.R = H;
   a.add_residual = add_residual ? 1 : 0;
-  return launch_expert_type<true>(type, a, s);
+  const qg_status r = launch_expert_type<true>(type, a, s);
+  if (r != QG_OK) return r;
+  if (!qg::aligned16(x_inout) || H % 4) return QG_EALIGN;
+  return qg::moe_launch_combine(a.dn, weights, ids, slots, n_slots, E, T, k, H, x_inout, add_residual ? 1 : 0, s);
 }
 
 }  // namespace

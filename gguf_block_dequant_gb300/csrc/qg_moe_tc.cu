@@ -557,6 +557,18 @@ qg_status moe_swiglu_tc(const void *w_gate, const void *w_up, int64_t stride, co
   return launch_tc_gemm<true>(mg, mu, mx, a, s);
 }
 
+qg_status moe_launch_combine(const float *dn, const float *weights, const int32_t *ids, const int32_t *slots,
+                             int n_slots, int E, int T, int k, int H, float *x_inout, int add_residual,
+                             cudaStream_t s) {
+  const qg::DeviceInfo &dev = qg::device_info();
+  const long long work = static_cast<long long>(T) * (H / 4);
+  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(4LL * dev.sms, (work + 127) / 128)));
+  return qg::launch_pdl(moe_tc_combine_kernel, dim3(grid), dim3(128), 0, s, dn, weights, ids, slots, n_slots, E, T, k,
+                        H, x_inout, add_residual) == cudaSuccess
+             ? QG_OK
+             : QG_ECUDA;
+}
+
 qg_status moe_combine_tc(const void *w_down, int64_t stride, const int32_t *slots, int n_slots, int E,
                          const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
                          float *x_inout, int add_residual, float *dn, void *ws, cudaStream_t s) {
@@ -585,13 +597,7 @@ qg_status moe_combine_tc(const void *w_down, int64_t stride, const int32_t *slot
   a.dn = dn;
   r = launch_tc_gemm<false>(md, md, mx, a, s);
   if (r != QG_OK) return r;
-  const qg::DeviceInfo &dev = qg::device_info();
-  const long long work = static_cast<long long>(T) * (H / 4);
-  const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(4LL * dev.sms, (work + 255) / 256)));
-  return qg::launch_pdl(moe_tc_combine_kernel, dim3(grid), dim3(256), 0, s, static_cast<const float *>(dn), weights,
-                        ids, slots, n_slots, E, T, k, H, x_inout, add_residual) == cudaSuccess
-             ? QG_OK
-             : QG_ECUDA;
+  return moe_launch_combine(dn, weights, ids, slots, n_slots, E, T, k, H, x_inout, add_residual, s);
 }
 
 }  // namespace qg

@@ -132,8 +132,10 @@ QG_API qg_status qgemm(int type, const void *w, const float *x, float *y, int64_
  * Pairs z = t*k + j index the per-pick buffers (act is f32 [T*k][F]).
  *
  * Workspace: moe_workspace_size(T, k, E, H, F) bytes of device memory, 16-byte aligned,
- * zero-filled by the caller once before its first use; every call leaves the workspace's
- * counters at zero again.  Calls that share a workspace must not run concurrently. */
+ * zero-filled by the caller once before its first use (it holds the router's per-tile
+ * tickets, which every call leaves at zero again); it also holds the router logits, the
+ * per-pick down rows and, for more than 16 tokens, the grouped bf16 rows.  Calls that share a
+ * workspace must not run concurrently. */
 QG_API size_t moe_workspace_size(int T, int k, int E, int H, int F);
 
 /* Router (matmulF32 + topk / topkB): logits l[t][e] = sum_h wr[e][h] * xn[t][h] (f32

@@ -65,10 +65,9 @@ def test_moe_host_checks_need_no_gpu(lib):
     lib.moe_route_topk.argtypes = [P, P, I, I, I, I, P, P, P, P, SZ, P]
     lib.moe_expert_swiglu.argtypes = [I, P, P, I64, P, I, I, P, P, I, I, I, I, P, P, SZ, P]
     lib.moe_combine.argtypes = [I, P, I64, P, I, I, P, P, P, I, I, I, I, P, I, P, SZ, P]
-    # workspace: logits + tickets + dn + counters (one per token and 2-row block), each rounded
-    # to 256 bytes
+    # workspace: router logits + tickets + dn rows, each rounded to 256 bytes
     n = lib.moe_workspace_size(8, 8, 128, 2048, 768)
-    assert n == 4096 + 256 + 8 * 8 * 2048 * 4 + 8 * 1024 * 4
+    assert n == 4096 + 256 + 8 * 8 * 2048 * 4
     assert lib.moe_workspace_size(8, 33, 128, 2048, 768) == 0   # k > 32
     assert lib.moe_workspace_size(8, 8, 300, 2048, 768) == 0    # E > 256
     fake = P(4096)
