@@ -4,9 +4,10 @@
 One step is one decode pass over the projections of a Qwen3-4B-shaped dense model in Q8_0:
 36 layers x (attn_q 4096x2560, attn_k 1024x2560, attn_v 1024x2560, attn_output 2560x4096,
 ffn_gate 9728x2560, ffn_up 9728x2560, ffn_down 2560x9728) plus the tied output head
-151936x2560, i.e. 253 GEMV launches and 4.27 GB of distinct raw GGUF blocks per step (far
-larger than the 129 MB L2, so every step streams its weights from HBM).  Every layer holds its
-own copy of the synthetic weight bytes at its own address.
+151936x2560: 4.27 GB of distinct raw GGUF blocks per step (far larger than the 129 MB L2, so
+every step streams its weights from HBM).  Every layer holds its own copy of the synthetic
+weight bytes at its own address.  Projections that read the same input share one launch
+(qgemv_multi: q, k, v; gate, up), so a step is 36 x 4 + 1 = 145 GEMV launches.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--tokens T] [--sections main|all]
     python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
@@ -14,7 +15,7 @@ own copy of the synthetic weight bytes at its own address.
 Prints ONE JSON line (rank 0).  ``value`` is weight bytes / device time with everything
 resident in HBM; ``e2e`` is the same metric through the public binding with the step's input
 activations copied from pinned host memory and the head's logits copied back, every step.
-The step is captured once in a CUDA graph and replayed (253 launches per replay).
+The step is captured once in a CUDA graph and replayed.
 With ``--sections all`` a ``detail`` object adds T = 4 / 16, per-projection times, the
 K-quant and Q4_0 shapes, the MoE layer and the T = 512 prefill GEMM.  Multi-GPU: replicas only (each rank runs the
 same step on its own GPU; no data-path collective).
@@ -79,7 +80,7 @@ def workload_config(args, layers=None):
         "activations": "f32 N(0,1), token-major [T][N]",
         "tokens": args.tokens,
         "layers": layers,
-        "launches_per_step": 7 * layers + 1,
+        "launches_per_step": 4 * layers + 1,
         "weight_bytes_per_step": step_weight_bytes(layers),
         "l2": "inputs larger than L2: every step streams its own 4.27 GB of distinct weights",
         "parallelism": f"replicas x{args.gpus}",
@@ -280,11 +281,17 @@ class Decode:
         else:
             self.qg.qgemv_t(gs.Q8_0, wt, self.x[N], self.y[name], M, N, T)
 
+    def multi(self, names, l, T):
+        N = gs.QWEN3_4B_PROJ[names[0]][1]
+        self.qg.qgemv_multi(gs.Q8_0, [self.w[n][l] for n in names], [self.y[n] for n in names], self.x[N], N, T)
+
     def step(self, T=None):
         T = self.T if T is None else T
         for l in range(self.layers):
-            for name in PROJ:
-                self.gemv(name, self.w[name][l], T)
+            self.multi(("attn_q", "attn_k", "attn_v"), l, T)
+            self.gemv("attn_output", self.w["attn_output"][l], T)
+            self.multi(("ffn_gate", "ffn_up"), l, T)
+            self.gemv("ffn_down", self.w["ffn_down"][l], T)
         self.gemv(HEAD, self.w[HEAD][0], T)
 
 
@@ -367,7 +374,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(device=dev)
     wbytes = step_weight_bytes(args.layers)
     abytes = step_act_bytes(args.layers, T)
-    launches = 7 * args.layers + 1
+    launches = 4 * args.layers + 1
 
     g = capture(torch, lambda: D.step(T), stream)
     if qg.device_status() != 0:

@@ -54,6 +54,7 @@ def load():
             "qgemv_q4_k": ([P, P, P, I64, I64, S], I),
             "qgemv_q6_k": ([P, P, P, I64, I64, S], I),
             "qgemv_t": ([I, P, P, P, I64, I64, I, S], I),
+            "qgemv_multi": ([I, I, P, P, P, I64, P, I, S], I),
             "qgemm_workspace_size": ([I, I64, I64, I64], SZ),
             "qgemm": ([I, P, P, P, I64, I64, I64, P, SZ, S], I),
             "moe_workspace_size": ([I, I, I, I, I], SZ),
@@ -144,6 +145,19 @@ def qgemv_t(qtype, w, x, y, M, N, T, stream=None):
     """Y[t][m] = W[m] . X[t] for T <= 16 token rows, one weight pass."""
     _call("qgemv_t", qtype, _ptr(w), _ptr(x), _ptr(y), M, N, T, _stream(stream))
     return y
+
+
+def qgemv_multi(qtype, ws, ys, x, N, T, stream=None):
+    """Y_j = W_j . X for up to 4 matrices sharing the activations X [T][N], one launch.
+    ws: weight tensors (raw blocks), ys: f32 [T][M_j] outputs; M_j from ys."""
+    n = len(ws)
+    if n != len(ys):
+        raise ValueError("one output per weight tensor")
+    W = (ctypes.c_void_p * n)(*[w.data_ptr() for w in ws])
+    Y = (ctypes.c_void_p * n)(*[y.data_ptr() for y in ys])
+    M = (ctypes.c_int64 * n)(*[int(y.shape[-1]) for y in ys])
+    _call("qgemv_multi", qtype, n, W, Y, M, N, _ptr(x), T, _stream(stream))
+    return ys
 
 
 def qgemm_workspace_size(qtype, M, N, T) -> int:

@@ -29,6 +29,7 @@ const DeviceInfo &device_info() {
     DeviceInfo &d = g_info[dev];
     d.ok = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+           cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
            cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) == cudaSuccess;
   });
   return g_info[dev];
@@ -49,6 +50,9 @@ bool set_smem_attr(const void *func, uint32_t bytes) {
     }
   if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) != cudaSuccess)
     return false;
+  // the whole unified L1/shared array as shared memory: every kernel here stages its operands
+  // there, and two-CTA-per-SM launches need the full carveout
+  cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (g_attr_n < 256) g_attr[g_attr_n++] = AttrEntry{func, dev, bytes};
   return true;
 }

@@ -35,12 +35,18 @@ namespace {
 
 constexpr int kMaxNS = 4;  // slots per warp
 
+constexpr int kMaxMats = 4;  // matrices that one launch may cover (sharing x)
+
 struct GemvArgs {
-  const uint8_t *w;
-  float *y;
+  // up to kMaxMats matrices of the same type and row length over the same activations: their
+  // row blocks are numbered one after another (matrix j owns [rb0[j], rb0[j + 1]))
+  const uint8_t *w[kMaxMats];
+  float *y[kMaxMats];
+  int Mj[kMaxMats];
+  long long rb0[kMaxMats + 1];
+  int nmat;
   long long row_bytes;
-  long long total_bytes;
-  int M, N, T;
+  int N, T;
   int mode;          // 0: activations resident; 1: activations in K chunks (one per weight chunk)
   int KC;            // elements per weight chunk (multiple of SG)
   int nchunks;       // chunks per row
@@ -52,11 +58,36 @@ struct GemvArgs {
   int seg_slot;      // bytes per row segment inside a slot; 0: the block's whole rows in one copy
   int box_rows;      // rows per activation tensor copy
   int maxq;          // most row blocks of one warp (mode 1 partial sums)
+  long long prefetch_bytes;  // weight bytes of its range each CTA pulls into L2 before its wait
   uint32_t off_x, off_ring, off_red, off_part;
   uint32_t xbuf_bytes;
 };
 
 QG_DEVICE void set_status(unsigned int bits) { atomicOr(&g_qg_status_gemv, bits); }
+
+// The matrix that owns row block rb, and the block's index within it.
+struct RowBlock {
+  const uint8_t *w;
+  float *y;
+  int M;
+  long long lrb;
+  uintptr_t mend;  // last 16-byte boundary of the matrix
+};
+
+QG_DEVICE RowBlock row_block(const GemvArgs &a, long long rb) {
+  int j = 0;
+#pragma unroll
+  for (int q = 1; q < kMaxMats; ++q)
+    if (q < a.nmat && rb >= a.rb0[q]) j = q;
+  RowBlock b;
+  b.w = a.w[j];
+  b.y = a.y[j];
+  b.M = a.Mj[j];
+  b.lrb = rb - a.rb0[j];
+  b.mend = (reinterpret_cast<uintptr_t>(b.w) + static_cast<uintptr_t>(static_cast<long long>(b.M) * a.row_bytes)) &
+           ~static_cast<uintptr_t>(15);
+  return b;
+}
 
 // Item cursor of one warp: tile index q (within the CTA) and chunk c.
 struct Cursor {
@@ -71,7 +102,7 @@ __host__ __device__ constexpr int rows_per_block() {
 }
 
 template <int QT, int TT, int NW>
-__global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant__ CUtensorMap xmap, const GemvArgs a) {
+__global__ void __launch_bounds__(NW * 32, (TT == 1) ? 2 : 1) qgemv_kernel(const __grid_constant__ CUtensorMap xmap, const GemvArgs a) {
   using D = Dec<QT>;
   constexpr int RR = rows_per_block<TT>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -104,6 +135,19 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
     mbar_init(&xfull[0], 1);
     mbar_init(&xfull[1], 1);
     fence_mbar_init();
+    // While the preceding kernel drains, pull the start of this CTA's weight rows into L2.
+    // (Only a hint: L2 is where coherence lives, so this cannot observe stale data, and the
+    // copies into shared memory below still wait for the predecessor.)
+    const RowBlock b0 = row_block(a, rbA);
+    const uintptr_t lo =
+        (reinterpret_cast<uintptr_t>(b0.w) + static_cast<uintptr_t>(b0.lrb * RR * a.row_bytes)) & ~static_cast<uintptr_t>(15);
+    const uintptr_t hi_all = b0.mend;
+    const uintptr_t want = lo + static_cast<uintptr_t>(a.prefetch_bytes);
+    const uintptr_t hi = want < hi_all ? want : hi_all;
+    for (uintptr_t p = lo; p < hi; p += 32768) {
+      const uint32_t n = static_cast<uint32_t>((hi - p) < 32768 ? (hi - p) : 32768);
+      bulk_prefetch_l2(reinterpret_cast<const void *>(p), n);
+    }
   }
   pdl_wait();
   pdl_launch_dependents();
@@ -132,8 +176,6 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
   auto valid = [&](Cursor u) { return a.mode == 0 ? u.q < my_rbs : u.c < a.nchunks; };
   auto rb_of = [&](Cursor u) { return rbA + rbl + static_cast<long long>(u.q) * nslots; };
 
-  const uintptr_t wbase = reinterpret_cast<uintptr_t>(a.w);
-  const uintptr_t mend = (wbase + static_cast<uintptr_t>(a.total_bytes)) & ~static_cast<uintptr_t>(15);
   const long long chunk_bytes = static_cast<long long>(a.KC / D::QK) * D::BB;
   uint8_t *wring = ring + warp * a.NS * a.stage_bytes;
   const uint32_t wring_s = smem_u32(wring);
@@ -143,8 +185,10 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
   // mbarrier before any copy starts.
   const bool pad_rows = a.seg_slot != 0;
   auto issue = [&](Cursor u, int s) {
-    const long long rb = rb_of(u);
-    const int nr = (my_rbs == 0) ? 0 : static_cast<int>(max(0LL, min(static_cast<long long>(RR), a.M - rb * RR)));
+    const RowBlock b = row_block(a, rb_of(u));
+    const uintptr_t wbase = reinterpret_cast<uintptr_t>(b.w);
+    const long long rb = b.lrb;
+    const int nr = (my_rbs == 0) ? 0 : static_cast<int>(max(0LL, min(static_cast<long long>(RR), b.M - rb * RR)));
     uint8_t *st = wring + s * a.stage_bytes;
     uintptr_t src = 0;
     uint32_t n = 0;
@@ -160,7 +204,7 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
       src = wbase + static_cast<uintptr_t>((rb * RR + lane) * a.row_bytes + u.c * chunk_bytes);
       dst = st + lane * a.seg_slot;
     }
-    warp_bulk_copies(dst, src, n, mend, &wbar[warp * kMaxNS + s], lane);
+    warp_bulk_copies(dst, src, n, b.mend, &wbar[warp * kMaxNS + s], lane);
   };
 
   // prologue: the first NS - 1 items
@@ -201,7 +245,7 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
       cur_xc = cc.c;
       if (ok && !mbar_wait(&xfull[cur_xc & 1], (cur_xc >> 1) & 1)) ok = false;
     }
-    const long long rb = rb_of(cc);
+    const RowBlock blk = row_block(a, rb_of(cc));
     const bool first_chunk = (a.mode == 1) || (cc.c == kw);
     const bool last_chunk = (a.mode == 1) || (cc.c + KW >= a.nchunks);
     if (first_chunk) {
@@ -220,7 +264,8 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
       uint32_t wrow[RR];
       {
         // low 32 bits suffice: only the address modulo 16 matters
-        const uint32_t r0 = static_cast<uint32_t>(wbase) + static_cast<uint32_t>(rb * RR) * static_cast<uint32_t>(a.row_bytes);
+        const uint32_t r0 = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(blk.w)) +
+                            static_cast<uint32_t>(blk.lrb * RR) * static_cast<uint32_t>(a.row_bytes);
         const uint32_t cb = static_cast<uint32_t>(cc.c) * static_cast<uint32_t>(chunk_bytes);
 #pragma unroll
         for (int r = 0; r < RR; ++r) {
@@ -307,8 +352,8 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
             if (cc.c > 0) val += pacc[idx];
             if (!final_chunk) pacc[idx] = val;
           }
-          const long long row = rb * RR + r;
-          if (own && final_chunk && ok && t < a.T && row < a.M) a.y[static_cast<long long>(t) * a.M + row] = val;
+          const long long row = blk.lrb * RR + r;
+          if (own && final_chunk && ok && t < a.T && row < blk.M) blk.y[static_cast<long long>(t) * blk.M + row] = val;
         }
       } else {
         float *myred = red + ((cc.q & 1) * NW + warp) * NV;  // double-buffered by row block
@@ -322,8 +367,8 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
             const int r = idx / TT, t = idx - r * TT;
             float sum = 0.f;
             for (int k = 0; k < KW; ++k) sum += base[k * NV + idx];
-            const long long row = rb * RR + r;
-            if (ok && t < a.T && row < a.M) a.y[static_cast<long long>(t) * a.M + row] = sum;
+            const long long row = blk.lrb * RR + r;
+            if (ok && t < a.T && row < blk.M) blk.y[static_cast<long long>(t) * blk.M + row] = sum;
           }
         }
       }
@@ -343,22 +388,36 @@ __global__ void __launch_bounds__(NW * 32, 1) qgemv_kernel(const __grid_constant
 // ------------------------------------------------------------------------------------------
 
 template <int QT, int TT>
-qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N, int T, cudaStream_t stream) {
+qg_status launch_t(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
+                   int T, cudaStream_t stream) {
   using D = Dec<QT>;
-  constexpr int NW = (TT == 1) ? 16 : 8;
+  // One token: CTAs of 8 warps, two per SM (half the shared memory each), so that the next
+  // kernel's CTAs can already sit on an SM while this kernel's last CTAs drain.
+  constexpr int NW = 8;
+  constexpr int CPS = (TT == 1) ? 2 : 1;  // CTAs per SM
   const qg::DeviceInfo &dev = qg::device_info();
   if (!dev.ok) return QG_ECUDA;
   const int ngroups = static_cast<int>((N + D::SG - 1) / D::SG);
   const long long row_bytes = N / D::QK * D::BB;
-  const long long budget = dev.smem_optin - 4096;
+  const long long budget = (CPS == 1) ? dev.smem_optin - 4096 : dev.smem_per_sm / CPS - 4096;
   const uint32_t hdr = 1024;
   constexpr int RR = rows_per_block<TT>();
   const uint32_t red_bytes = 2 * NW * RR * TT * 4;
   const long long xres = ((static_cast<long long>(T) * ngroups * D::SG * 4 + 1023) / 1024) * 1024;
 
   GemvArgs a{};
-  const long long rblocks = (M + RR - 1) / RR;
-  const long long rb_per_cta = (rblocks + dev.sms - 1) / dev.sms;
+  long long rblocks = 0;
+  for (int j = 0; j < nmat; ++j) {
+    a.w[j] = static_cast<const uint8_t *>(w[j]);
+    a.y[j] = y[j];
+    a.Mj[j] = static_cast<int>(Ms[j]);
+    a.rb0[j] = rblocks;
+    rblocks += (Ms[j] + RR - 1) / RR;
+  }
+  for (int j = nmat; j <= kMaxMats; ++j) a.rb0[j] = rblocks;
+  a.nmat = nmat;
+  const long long grid_ctas = std::min<long long>(rblocks, static_cast<long long>(CPS) * dev.sms);
+  const long long rb_per_cta = (rblocks + grid_ctas - 1) / grid_ctas;
   // activations resident (mode 0) when that still leaves the warps a ring of >= 48 KB
   int mode = (xres + 48 * 1024 <= budget - hdr - red_bytes - 1024) ? 0 : 1;
   int gpc = 0, NS = 0, seg_slot = 0;
@@ -427,11 +486,7 @@ qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N
     NS = static_cast<int>(std::min<long long>(kMaxNS, (budget - hdr - red_bytes - xbuf - 1024) / (static_cast<long long>(NW) * stage)));
     if (NS < 2) return QG_EUNSUPPORTED;
   }
-  a.w = static_cast<const uint8_t *>(w);
-  a.y = y;
   a.row_bytes = row_bytes;
-  a.total_bytes = row_bytes * M;
-  a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.T = T;
   a.mode = mode;
@@ -470,23 +525,62 @@ qg_status launch_t(const void *w, const float *x, float *y, int64_t M, int64_t N
 
   auto kern = qgemv_kernel<QT, TT, NW>;
   if (!qg::set_smem_attr(reinterpret_cast<const void *>(kern), smem)) return QG_ECUDA;
-  const int grid = static_cast<int>(std::min<long long>(rblocks, dev.sms));
+  const int grid = static_cast<int>(grid_ctas);
+  a.prefetch_bytes = std::min<long long>(static_cast<long long>(NW) * NS * stage, 256LL * 1024);
   if (qg::launch_pdl(kern, dim3(grid), dim3(NW * 32), smem, stream, map, a) != cudaSuccess) return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 
 template <int QT>
-qg_status launch_type(const void *w, const float *x, float *y, int64_t M, int64_t N, int T, cudaStream_t s) {
-  if (T == 1) return launch_t<QT, 1>(w, x, y, M, N, T, s);
-  if (T <= 2) return launch_t<QT, 2>(w, x, y, M, N, T, s);
-  if (T <= 4) return launch_t<QT, 4>(w, x, y, M, N, T, s);
-  if (T <= 8) return launch_t<QT, 8>(w, x, y, M, N, T, s);
-  return launch_t<QT, 16>(w, x, y, M, N, T, s);
+qg_status launch_type(int n, const void *const *w, const float *x, float *const *y, const int64_t *M, int64_t N, int T,
+                      cudaStream_t s) {
+  if (T == 1) return launch_t<QT, 1>(n, w, x, y, M, N, T, s);
+  if (T <= 2) return launch_t<QT, 2>(n, w, x, y, M, N, T, s);
+  if (T <= 4) return launch_t<QT, 4>(n, w, x, y, M, N, T, s);
+  if (T <= 8) return launch_t<QT, 8>(n, w, x, y, M, N, T, s);
+  return launch_t<QT, 16>(n, w, x, y, M, N, T, s);
 }
 
 }  // namespace
 
 namespace qg {
+
+qg_status gemv_multi_dispatch(int type, int n, const void *const *w, const float *x, float *const *y,
+                              const int64_t *M, int64_t N, int T, cudaStream_t s) {
+  int qk = 0, bb = 0;
+  if (qg_block_shape(type, &qk, &bb) != QG_OK) return QG_EUNSUPPORTED;
+  if (n < 1 || n > kMaxMats) return QG_EINVAL_SHAPE;
+  if (!w || !y || !M || !x) return QG_EINVAL_PTR;
+  if (N <= 0 || N % qk || T < 1 || T > 16 || N > INT32_MAX) return QG_EINVAL_SHAPE;
+  if (static_cast<long long>(T) * N > INT32_MAX) return QG_EINVAL_SHAPE;
+  if (!aligned16(x)) return QG_EALIGN;
+  // matrices with no rows are dropped; the rest keep their order
+  const void *ww[kMaxMats];
+  float *yy[kMaxMats];
+  int64_t mm[kMaxMats];
+  int k = 0;
+  long long rows = 0;
+  for (int j = 0; j < n; ++j) {
+    if (M[j] < 0 || M[j] > INT32_MAX) return QG_EINVAL_SHAPE;
+    if (M[j] == 0) continue;
+    if (!w[j] || !y[j]) return QG_EINVAL_PTR;
+    if (!aligned16(w[j]) || !aligned16(y[j])) return QG_EALIGN;
+    ww[k] = w[j];
+    yy[k] = y[j];
+    mm[k] = M[j];
+    rows += M[j];
+    ++k;
+  }
+  if (k == 0) return QG_OK;
+  if (rows > INT32_MAX) return QG_EINVAL_SHAPE;
+  switch (type) {
+    case QG_TYPE_Q8_0: return launch_type<QG_TYPE_Q8_0>(k, ww, x, yy, mm, N, T, s);
+    case QG_TYPE_Q4_0: return launch_type<QG_TYPE_Q4_0>(k, ww, x, yy, mm, N, T, s);
+    case QG_TYPE_Q4_K: return launch_type<QG_TYPE_Q4_K>(k, ww, x, yy, mm, N, T, s);
+    case QG_TYPE_Q6_K: return launch_type<QG_TYPE_Q6_K>(k, ww, x, yy, mm, N, T, s);
+    default: return QG_EUNSUPPORTED;
+  }
+}
 
 qg_status gemv_dispatch(int type, const void *w, const float *x, float *y, int64_t M, int64_t N, int T,
                         cudaStream_t s) {
@@ -497,13 +591,7 @@ qg_status gemv_dispatch(int type, const void *w, const float *x, float *y, int64
   if (static_cast<long long>(T) * N > INT32_MAX) return QG_EINVAL_SHAPE;
   if (!aligned16(w) || !aligned16(x) || !aligned16(y)) return QG_EALIGN;
   if (M == 0) return QG_OK;
-  switch (type) {
-    case QG_TYPE_Q8_0: return launch_type<QG_TYPE_Q8_0>(w, x, y, M, N, T, s);
-    case QG_TYPE_Q4_0: return launch_type<QG_TYPE_Q4_0>(w, x, y, M, N, T, s);
-    case QG_TYPE_Q4_K: return launch_type<QG_TYPE_Q4_K>(w, x, y, M, N, T, s);
-    case QG_TYPE_Q6_K: return launch_type<QG_TYPE_Q6_K>(w, x, y, M, N, T, s);
-    default: return QG_EUNSUPPORTED;
-  }
+  return gemv_multi_dispatch(type, 1, &w, x, &y, &M, N, T, s);
 }
 
 unsigned int read_status_gemv(bool clear) {
@@ -534,6 +622,10 @@ qg_status qgemv_q6_k(const void *w, const float *x, float *y, int64_t M, int64_t
 }
 qg_status qgemv_t(int type, const void *w, const float *x, float *y, int64_t M, int64_t N, int T, qg_stream_t s) {
   return qg::gemv_dispatch(type, w, x, y, M, N, T, reinterpret_cast<cudaStream_t>(s));
+}
+qg_status qgemv_multi(int type, int n, const void *const *w, float *const *y, const int64_t *M, int64_t N,
+                      const float *x, int T, qg_stream_t s) {
+  return qg::gemv_multi_dispatch(type, n, w, x, y, M, N, T, reinterpret_cast<cudaStream_t>(s));
 }
 
 }  // extern "C"

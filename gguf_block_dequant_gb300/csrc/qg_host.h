@@ -14,6 +14,7 @@ struct DeviceInfo {
   bool ok = false;
   int sms = 0;         // streaming multiprocessors
   int smem_optin = 0;  // max dynamic shared memory per block (opt-in)
+  int smem_per_sm = 0; // shared memory per SM
   int l2_bytes = 0;
 };
 
@@ -62,6 +63,8 @@ qg_status moe_combine_tc(const void *w_down, int64_t stride, const int32_t *slot
                          const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
                          float *x_inout, int add_residual, float *dn, void *ws, cudaStream_t s);
 
+qg_status gemv_multi_dispatch(int type, int n, const void *const *w, const float *x, float *const *y,
+                              const int64_t *M, int64_t N, int T, cudaStream_t s);
 unsigned int read_status_gemv(bool clear);
 unsigned int read_status_moetc(bool clear);
 unsigned int read_status_moe(bool clear);

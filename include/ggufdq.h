@@ -109,6 +109,16 @@ QG_API qg_status qgemv_q6_k(const void *w, const float *x, float *y, int64_t M, 
 QG_API qg_status qgemv_t(int type, const void *w, const float *x, float *y, int64_t M, int64_t N, int T,
                   qg_stream_t stream);
 
+/* ---- several matrices over the same activations, one launch ------------------------------
+ * Y_j[t][m] = sum_k W_j[m][k] * X[t][k] for j < n (n <= 4), every W_j of the same type and row
+ * length N, X shared.  The decode steps whose projections read one normalised input (q, k and
+ * v of attention; gate and up of the FFN) stream all their rows in a single pass of the
+ * kernel instead of one launch each.  w, y and M are HOST arrays of n entries (device pointers
+ * to raw blocks and f32 [T][M_j] outputs, row counts); a matrix with M_j == 0 is skipped.
+ * Same shape and alignment rules as qgemv_t. */
+QG_API qg_status qgemv_multi(int type, int n, const void *const *w, float *const *y, const int64_t *M, int64_t N,
+                      const float *x, int T, qg_stream_t stream);
+
 /* ---- prefill dequant-GEMM, T >= 17 token rows --------------------------------------------
  * Y[t][m] = sum_k W[m][k] * X[t][k] with W decoded to bf16 and X rounded to bf16 for the
  * tensor cores, f32 accumulation (the tiled matmulQ8T generalised to a prefill chunk).

@@ -56,6 +56,13 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.qgemv_t(13, fake, fake, fake, 4, 64, 1, None) == 4  # unsupported type
     odd = P(4096 + 2)
     assert lib.qgemv_q8_0(odd, fake, fake, 4, 64, None) == 3       # misaligned weights
+    lib.qgemv_multi.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, I64, P, ctypes.c_int, P]
+    W = (P * 2)(fake, fake)
+    Y = (P * 2)(fake, fake)
+    M = (I64 * 2)(4, 4)
+    assert lib.qgemv_multi(8, 5, W, Y, M, 64, fake, 1, None) == 1  # n > 4
+    assert lib.qgemv_multi(8, 2, W, Y, M, 48, fake, 1, None) == 1  # N % 32 != 0
+    assert lib.qgemv_multi(8, 2, None, Y, M, 64, fake, 1, None) == 2
 
 
 def test_moe_host_checks_need_no_gpu(lib):

@@ -161,3 +161,33 @@ def test_config1_full(qg, oracle_lib):
     y = _run(qg, gs.Q8_0, w, x, M, N)
     ref, bnd = oracle_lib.gemv(gs.Q8_0, w, M, N, x, threads=4)
     assert_within_bound(y, ref, bnd, what="config 1")
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("T", [1, 3, 16])
+def test_gemv_multi_matches_separate_calls(qg, oracle_lib, qtype, T):
+    """qgemv_multi over matrices of different heights (one empty) equals the oracle per matrix."""
+    N = 1024 if gs.BLOCK[qtype][0] == 32 else 2048
+    Ms = [130, 37, 0, 261]
+    x = gs.activations(T, N, seed=T, stream=71)
+    ws = [gs.quant_blocks(qtype, max(M, 1), N, seed=j, stream=80 + j) for j, M in enumerate(Ms)]
+    wd = [to_dev(w, torch) for w in ws]
+    yd = [torch.full((T, max(M, 1)), float("nan"), dtype=torch.float32, device="cuda")[:, :M] for M in Ms]
+    yd = [y.contiguous() for y in yd]
+    qg.qgemv_multi(qtype, wd, yd, to_dev(x, torch), N, T)
+    torch.cuda.synchronize()
+    assert qg.device_status() == 0
+    for j, M in enumerate(Ms):
+        if M == 0:
+            continue
+        ref, bnd = oracle_lib.gemv(qtype, ws[j], M, N, x, threads=4)
+        assert_within_bound(yd[j].cpu().numpy(), ref, bnd, what=f"multi type {qtype} j={j} T={T}")
+
+
+def test_gemv_multi_rejects(qg):
+    w = torch.zeros(34 * 64, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(256, dtype=torch.float32, device="cuda")
+    y = torch.zeros((1, 8), dtype=torch.float32, device="cuda")
+    with pytest.raises(qg.QGError) as e:
+        qg.qgemv_multi(gs.Q8_0, [w] * 5, [y] * 5, x, 256, 1)  # more than 4 matrices
+    assert e.value.status == qg.QG_EINVAL_SHAPE
