@@ -59,6 +59,7 @@ def load():
             "qgemm": ([I, P, P, P, I64, I64, I64, P, SZ, S], I),
             "moe_workspace_size": ([I, I, I, I, I], SZ),
             "moe_route_topk": ([P, P, I, I, I, I, P, P, P, P, SZ, S], I),
+            "moe_route_topk_noalloc": ([P, P, I, I, I, I, P, P, P, S], I),
             "moe_expert_swiglu": ([I, P, P, I64, P, I, I, P, P, I, I, I, I, P, P, SZ, S], I),
             "moe_combine": ([I, P, I64, P, I, I, P, P, P, I, I, I, I, P, I, P, SZ, S], I),
             "moe_layer": ([I, P, P, P, P, P, I64, P, I, I, I, I, I, I, P, P, P, P, P, SZ, S], I),
@@ -183,6 +184,13 @@ def _nbytes(t):
 def moe_route_topk(xn, wr, T, H, E, k, ids, weights, logits=None, workspace=None, stream=None):
     _call("moe_route_topk", _ptr(xn), _ptr(wr), T, H, E, k, _ptr(ids), _ptr(weights), _ptr(logits),
           _ptr(workspace), _nbytes(workspace), _stream(stream))
+    return ids, weights
+
+
+def moe_route_topk_noalloc(xn, wr, T, H, E, k, ids, weights, logits=None, stream=None):
+    """moe_route_topk without a workspace argument (library-held scratch, T * E <= 16384)."""
+    _call("moe_route_topk_noalloc", _ptr(xn), _ptr(wr), T, H, E, k, _ptr(ids), _ptr(weights), _ptr(logits),
+          _stream(stream))
     return ids, weights
 
 

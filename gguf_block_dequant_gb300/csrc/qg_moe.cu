@@ -26,6 +26,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 #include "qg_decode.cuh"
 #include "qg_host.h"
@@ -978,7 +979,49 @@ unsigned int read_status_moe(bool clear) {
 }
 }  // namespace qg
 
+// ---- router without a caller workspace -----------------------------------------------------
+// Fixed device scratch for moe_route_topk_noalloc: the router's logits and its per-tile
+// tickets, laid out exactly as the workspace of moe_route_topk.  Sized for T * E <= 16384
+// logits and 1024 token tiles (68 KB).
+namespace {
+constexpr int kNoAllocLogits = 16384;
+constexpr int kNoAllocTiles = 1024;
+constexpr size_t kNoAllocBytes = static_cast<size_t>(kNoAllocLogits) * 4 + static_cast<size_t>(kNoAllocTiles) * 4;
+__device__ __align__(256) unsigned char g_route_scratch[kNoAllocBytes];
+
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64];  // per device, filled on the first call with that device current
+
+void *route_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) return nullptr;
+    g_scratch_ptr[dev] = p;
+  }
+  return g_scratch_ptr[dev];
+}
+}  // namespace
+
 extern "C" {
+
+qg_status moe_route_topk_noalloc(const float *xn, const float *wr, int T, int H, int E, int k, int32_t *ids,
+                                 float *weights, float *logits_out, qg_stream_t stream) {
+  if (T < 1 || E < 1 || static_cast<long long>(T) * E > kNoAllocLogits ||
+      (T + kRouterTB - 1) / kRouterTB > kNoAllocTiles)
+    return QG_EWORKSPACE;
+  void *ws = route_scratch();
+  if (!ws) return QG_ECUDA;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(T, 1, E, H);
+  // the tickets must read zero when the router starts: clear them for this shape's layout
+  if (cudaMemsetAsync(static_cast<uint8_t *>(ws) + L.ticket, 0,
+                      static_cast<size_t>((T + kRouterTB - 1) / kRouterTB) * 4, s) != cudaSuccess)
+    return QG_ECUDA;
+  return route_impl(xn, wr, T, H, E, k, ids, weights, logits_out, ws, kNoAllocBytes, s);
+}
 
 size_t moe_workspace_size(int T, int k, int E, int H, int F) {
   if (check_common(T, k, E, H, F) != QG_OK) return 0;

@@ -158,6 +158,23 @@ QG_API qg_status moe_route_topk(const float *xn, const float *wr, int T, int H, 
                          float *weights, float *logits_out, void *workspace, size_t workspace_bytes,
                          qg_stream_t stream);
 
+/* The router of moe_route_topk for callers that cannot hand the library a workspace: for
+ * instance a host engine whose device memory is entirely reserved by its own allocator before
+ * it calls in, or a binding that exposes only input and output tensors.  The library keeps a
+ * fixed 68 KB scratch area in device memory for the logits and the per-tile tickets and
+ * allocates nothing (no cudaMalloc, no allocating library call).
+ *   - Limits: T * E <= 16384 and at most 1024 tiles of 16 tokens; larger shapes return
+ *     QG_EWORKSPACE.
+ *   - The scratch address is looked up once per device, on the first call with that device
+ *     current; make that first call before any stream capture.
+ *   - Each call clears the tickets of its shape on `stream` before the router runs.
+ *   - One scratch area per device: calls that overlap (other streams, other host threads)
+ *     race on it and must be serialised by the caller.
+ * Results are the same as moe_route_topk's.  The engine pages have no counterpart: their
+ * router buffers are allocated by the engine. */
+QG_API qg_status moe_route_topk_noalloc(const float *xn, const float *wr, int T, int H, int E, int k, int32_t *ids,
+                                 float *weights, float *logits_out, qg_stream_t stream);
+
 /* Gate/up expert rows with SwiGLU (expertQ8 with a shared input, then siluMulMoe): for each
  * pair z = t*k + j with expert e = ids[z]:  g = Wg[s] . xn[t],  u = Wu[s] . xn[t]  (F rows
  * each),  act[z][i] = g_i / (1 + exp(-g_i)) * u_i.  Experts are grouped so that each picked
