@@ -55,6 +55,10 @@ def parse():
     p.add_argument("--tokens", type=int, default=1, help="token columns T of the headline step (1..16)")
     p.add_argument("--layers", type=int, default=LAYERS)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--weights", choices=["static", "ordered"], default="static",
+                   help="static: the weights are immutable parameters, so each GEMV may start streaming "
+                        "them before its predecessor ends (qg_set_static_weights); ordered: every launch "
+                        "waits for its predecessor before it reads anything")
     p.add_argument("--sections", choices=["main", "all", "gemm", "moe", "kquant", "proj"], default="all",
                    help="main: the headline line only; all: plus the detail object; gemm / moe / kquant / "
                         "proj: only that detail section, printed as its own JSON line (for profiling runs)")
@@ -84,6 +88,7 @@ def workload_config(args, layers=None):
         "weight_bytes_per_step": step_weight_bytes(layers),
         "l2": "inputs larger than L2: every step streams its own 4.27 GB of distinct weights",
         "parallelism": f"replicas x{args.gpus}",
+        "weights_mode": getattr(args, "weights", "static"),
     }
 
 
@@ -376,6 +381,7 @@ def run_ours(args):
     abytes = step_act_bytes(args.layers, T)
     launches = 4 * args.layers + 1
 
+    qg.set_static_weights(args.weights == "static")
     g = capture(torch, lambda: D.step(T), stream)
     if qg.device_status() != 0:
         raise RuntimeError("device status set after the first step")
@@ -478,6 +484,16 @@ def run_detail(torch, qg, D, stream, args, hbm):
     """Secondary numbers: T = 4 / 16 steps, per-projection T = 1 times, K-quant shapes, MoE."""
     out = {}
     wbytes = step_weight_bytes(args.layers)
+    other = "ordered" if args.weights == "static" else "static"
+    prev = qg.set_static_weights(other == "static")
+    g = capture(torch, lambda: D.step(args.tokens), stream)
+    qg.set_static_weights(prev)
+    steps = max(20, args.steps // 4)
+    el = time_graph(torch, g, stream, steps, 3)
+    gbs = wbytes * steps / el / 1e9
+    out[f"decode_step_T{args.tokens}_{other}_weights"] = {"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+                                                         "us_per_step": round(el / steps * 1e6, 1)}
+    del g
     for T in (4, 16):
         if T == args.tokens:
             continue

@@ -49,6 +49,7 @@ def load():
             "qg_strerror": ([I], ctypes.c_char_p),
             "qg_block_shape": ([I, P, P], I),
             "qg_device_status": ([P, I], I),
+            "qg_set_static_weights": ([I], I),
             "qgemv_q8_0": ([P, P, P, I64, I64, S], I),
             "qgemv_q4_0": ([P, P, P, I64, I64, S], I),
             "qgemv_q4_k": ([P, P, P, I64, I64, S], I),
@@ -108,6 +109,12 @@ def device_status(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _call("qg_device_status", ctypes.byref(v), int(clear))
     return v.value
+
+
+def set_static_weights(enable: bool) -> bool:
+    """Declare the weight buffers immutable: GEMVs may start streaming them before the
+    preceding kernel in the stream finishes.  Returns the previous setting."""
+    return bool(load().qg_set_static_weights(int(bool(enable))))
 
 
 def row_bytes(qtype: int, n: int) -> int:

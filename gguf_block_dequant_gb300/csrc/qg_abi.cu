@@ -1,5 +1,6 @@
 // qg_abi.cu -- library-wide entry points: version, status strings, block shapes, device
 // status word, and the per-device property cache.
+#include <atomic>
 #include <mutex>
 
 #include "qg_host.h"
@@ -34,6 +35,12 @@ const DeviceInfo &device_info() {
   });
   return g_info[dev];
 }
+
+namespace {
+std::atomic<int> g_static_weights{0};
+}
+
+bool static_weights() { return g_static_weights.load(std::memory_order_relaxed) != 0; }
 
 bool set_smem_attr(const void *func, uint32_t bytes) {
   int dev = 0;
@@ -90,6 +97,10 @@ qg_status qg_block_shape(int type, int *qk, int *block_bytes) {
   if (qk) *qk = a;
   if (block_bytes) *block_bytes = b;
   return QG_OK;
+}
+
+int qg_set_static_weights(int enable) {
+  return qg::g_static_weights.exchange(enable ? 1 : 0) != 0;
 }
 
 qg_status qg_device_status(uint32_t *status_out, int clear) {

@@ -104,11 +104,6 @@ QG_DEVICE void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, ui
       : "memory");
 }
 
-// L2 prefetch of a global range (no completion tracking); size multiple of 16.
-QG_DEVICE void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
-}
-
 // 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned); completes at
 // cp_async_wait_all()
 QG_DEVICE void cp_async16(uint32_t dst_smem, const void *src) {

@@ -58,7 +58,7 @@ struct GemvArgs {
   int seg_slot;      // bytes per row segment inside a slot; 0: the block's whole rows in one copy
   int box_rows;      // rows per activation tensor copy
   int maxq;          // most row blocks of one warp (mode 1 partial sums)
-  long long prefetch_bytes;  // weight bytes of its range each CTA pulls into L2 before its wait
+  int early_weights;  // weights are static: issue the first weight stages before the wait on the predecessor
   uint32_t off_x, off_ring, off_red, off_part;
   uint32_t xbuf_bytes;
 };
@@ -135,25 +135,6 @@ __global__ void __launch_bounds__(NW * 32, (TT == 1) ? 2 : 1) qgemv_kernel(const
     mbar_init(&xfull[0], 1);
     mbar_init(&xfull[1], 1);
     fence_mbar_init();
-    // While the preceding kernel drains, pull the start of this CTA's weight rows into L2.
-    // (Only a hint: L2 is where coherence lives, so this cannot observe stale data, and the
-    // copies into shared memory below still wait for the predecessor.)
-    const RowBlock b0 = row_block(a, rbA);
-    const uintptr_t lo =
-        (reinterpret_cast<uintptr_t>(b0.w) + static_cast<uintptr_t>(b0.lrb * RR * a.row_bytes)) & ~static_cast<uintptr_t>(15);
-    const uintptr_t hi_all = b0.mend;
-    const uintptr_t want = lo + static_cast<uintptr_t>(a.prefetch_bytes);
-    const uintptr_t hi = want < hi_all ? want : hi_all;
-    for (uintptr_t p = lo; p < hi; p += 32768) {
-      const uint32_t n = static_cast<uint32_t>((hi - p) < 32768 ? (hi - p) : 32768);
-      bulk_prefetch_l2(reinterpret_cast<const void *>(p), n);
-    }
-  }
-  pdl_wait();
-  pdl_launch_dependents();
-  if (threadIdx.x == 0) {
-    load_x(xs, &xmap, a.T, a.N, 0, a.xR, a.box_rows, &xfull[0]);
-    if (a.mode == 1 && a.nchunks > 1) load_x(xs + a.xbuf_bytes, &xmap, a.T, a.N, 1, a.xR, a.box_rows, &xfull[1]);
   }
   __syncthreads();
 
@@ -207,15 +188,28 @@ __global__ void __launch_bounds__(NW * 32, (TT == 1) ? 2 : 1) qgemv_kernel(const
     warp_bulk_copies(dst, src, n, b.mend, &wbar[warp * kMaxNS + s], lane);
   };
 
-  // prologue: the first NS - 1 items
+  // Prologue: the first NS - 1 items.  Normally issued after the wait on the preceding kernel
+  // and after the activations; with static weights (the caller guarantees that no kernel
+  // writes them) they are issued as soon as the CTA is resident, while the preceding kernel
+  // drains, and only the activations and outputs wait.
   Cursor ic = first();
   int is = 0, issued = 0;
-  for (int i = 0; i < a.NS - 1 && valid(ic); ++i) {
-    issue(ic, is);
-    ic = next(ic);
-    is = (is + 1 == a.NS) ? 0 : is + 1;
-    ++issued;
+  auto prologue = [&]() {
+    for (int i = 0; i < a.NS - 1 && valid(ic); ++i) {
+      issue(ic, is);
+      ic = next(ic);
+      is = (is + 1 == a.NS) ? 0 : is + 1;
+      ++issued;
+    }
+  };
+  if (a.early_weights) prologue();
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    load_x(xs, &xmap, a.T, a.N, 0, a.xR, a.box_rows, &xfull[0]);
+    if (a.mode == 1 && a.nchunks > 1) load_x(xs + a.xbuf_bytes, &xmap, a.T, a.N, 1, a.xR, a.box_rows, &xfull[1]);
   }
+  if (!a.early_weights) prologue();
 
   const uint32_t wo = static_cast<uint32_t>(D::woff(lane));
   uint32_t xo[D::NCH];
@@ -526,7 +520,7 @@ qg_status launch_t(int nmat, const void *const *w, const float *x, float *const 
   auto kern = qgemv_kernel<QT, TT, NW>;
   if (!qg::set_smem_attr(reinterpret_cast<const void *>(kern), smem)) return QG_ECUDA;
   const int grid = static_cast<int>(grid_ctas);
-  a.prefetch_bytes = std::min<long long>(static_cast<long long>(NW) * NS * stage, 256LL * 1024);
+  a.early_weights = qg::static_weights() ? 1 : 0;
   if (qg::launch_pdl(kern, dim3(grid), dim3(NW * 32), smem, stream, map, a) != cudaSuccess) return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }

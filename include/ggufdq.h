@@ -92,6 +92,19 @@ QG_API qg_status qg_block_shape(int type, int *qk, int *block_bytes);
  * Synchronises the device.  When `clear` is non-zero the word is reset to 0. */
 QG_API qg_status qg_device_status(uint32_t *status_out, int clear);
 
+/* Static weights (process-wide switch, off by default).  Every launch of this library waits
+ * for the preceding kernel in its stream (programmatic dependent launch) before it touches
+ * memory.  A caller whose weight buffers are immutable model parameters - written once,
+ * before any GEMV that reads them, and never by a kernel enqueued ahead of a GEMV in the
+ * same stream - may call qg_set_static_weights(1): the dense GEMVs (qgemv_* and
+ * qgemv_multi) then start streaming their first weight tiles into shared memory while the
+ * preceding kernel drains, and only the activations and outputs wait for it.  Leave it off
+ * when a kernel in the stream may write the weights (quantise-in-place, a loader that copies
+ * through a kernel): the GEMV could read stale bytes.  Host-to-device copies are ordered
+ * either way.  Takes effect for launches enqueued after the call; returns the previous
+ * setting (0 or 1). */
+QG_API int qg_set_static_weights(int enable);
+
 /* ---- dense quantized GEMV, one token ----------------------------------------------------
  * y[m] = sum_k W[m][k] * x[k] for m < M  (matmulQ8 / matmulQ4 / matmulQ6K on the pages, and
  * the Q4_K row dot of WG_GEMM_Q4K).  w: M*N/QK raw blocks; x: f32[N]; y: f32[M].

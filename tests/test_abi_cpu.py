@@ -90,3 +90,16 @@ def test_moe_host_checks_need_no_gpu(lib):
                                  None) == 4  # unsupported type
     assert lib.moe_combine(8, fake, 0, None, 1, 8, fake, fake, fake, 2, 2, 64, 32, fake, 1, fake, 16,
                            None) == 8  # workspace too small
+
+
+def test_static_weights_switch_returns_previous_setting(lib):
+    lib.qg_set_static_weights.argtypes = [ctypes.c_int]
+    lib.qg_set_static_weights.restype = ctypes.c_int
+    prev = lib.qg_set_static_weights(0)
+    try:
+        assert lib.qg_set_static_weights(7) == 0  # any non-zero value enables it
+        assert lib.qg_set_static_weights(1) == 1
+        assert lib.qg_set_static_weights(0) == 1
+        assert lib.qg_set_static_weights(0) == 0
+    finally:
+        lib.qg_set_static_weights(prev)

@@ -191,3 +191,39 @@ def test_gemv_multi_rejects(qg):
     with pytest.raises(qg.QGError) as e:
         qg.qgemv_multi(gs.Q8_0, [w] * 5, [y] * 5, x, 256, 1)  # more than 4 matrices
     assert e.value.status == qg.QG_EINVAL_SHAPE
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_static_weights_chain_matches_default(qg, oracle_lib, T):
+    """With static weights on, each GEMV streams its weights before the preceding GEMV ends,
+    but its activations still come from that GEMV's output: a chain y_i -> x_(i+1) equals the
+    fully stream-ordered run bit for bit, and every link is within the oracle's bound."""
+    dims = [1024, 2048, 512, 1024, 1024]  # N_0, M_0 = N_1, ...
+    ws = [gs.quant_blocks(gs.Q8_0, dims[i + 1], dims[i], seed=i, stream=90) for i in range(len(dims) - 1)]
+    wd = [to_dev(w, torch) for w in ws]
+    x0 = to_dev(gs.activations(T, dims[0], seed=T, stream=91), torch)
+
+    def chain():
+        ys, x = [], x0
+        for i, w in enumerate(wd):
+            y = torch.empty((T, dims[i + 1]), dtype=torch.float32, device="cuda")
+            qg.qgemv_t(gs.Q8_0, w, x, y, dims[i + 1], dims[i], T)
+            ys.append(y)
+            x = y
+        torch.cuda.synchronize()
+        assert qg.device_status() == 0
+        return [y.cpu().numpy() for y in ys]
+
+    prev = qg.set_static_weights(False)
+    try:
+        base = chain()
+        qg.set_static_weights(True)
+        fast = chain()
+    finally:
+        qg.set_static_weights(prev)
+    xin = x0.cpu().numpy()
+    for i, (a, b) in enumerate(zip(base, fast)):
+        assert np.array_equal(a, b), f"link {i} differs"
+        ref, bnd = oracle_lib.gemv(gs.Q8_0, ws[i], dims[i + 1], dims[i], xin, threads=4)
+        assert_within_bound(b, ref, bnd, what=f"chain link {i} T={T}")
+        xin = b
