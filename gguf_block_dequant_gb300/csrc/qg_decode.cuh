@@ -90,17 +90,15 @@ struct Dec<QG_TYPE_Q8_0> {
   }
   QG_DEVICE static float xaux(const float4 *) { return 0.f; }
   QG_DEVICE static float dot1(const U &u, const float4 *xc, float) {
-    float s0 = 0.f, s1 = 0.f;
+    f2 s = mk2(0.f, 0.f);
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) {
       f2 q01, q23;
       codes(u, ch, q01, q23);
-      s0 = fmaf(q01.x, xc[ch].x, s0);
-      s1 = fmaf(q01.y, xc[ch].y, s1);
-      s0 = fmaf(q23.x, xc[ch].z, s0);
-      s1 = fmaf(q23.y, xc[ch].w, s1);
+      s = fma2(q01, mk2(xc[ch].x, xc[ch].y), s);
+      s = fma2(q23, mk2(xc[ch].z, xc[ch].w), s);
     }
-    return u.d * (s0 + s1);
+    return u.d * (s.x + s.y);
   }
 };
 
@@ -140,22 +138,18 @@ struct Dec<QG_TYPE_Q4_0> {
   // one-token dot: the high nibbles are used in place (byte & 0xF0 = 16 q), which gives
   // 16 (q - 8) after subtracting 2^23 + 128; their sum is scaled by 1/16 (exact)
   QG_DEVICE static float dot1(const U &u, const float4 *xc, float) {
-    float lo0 = 0.f, lo1 = 0.f, hi0 = 0.f, hi1 = 0.f;
+    f2 lo = mk2(0.f, 0.f), hi = mk2(0.f, 0.f);
 #pragma unroll
     for (int ch = 0; ch < 2; ++ch) {
       f2 q01, q23;
       magic4(u.c[ch] & 0x0F0F0F0Fu, -8388616.0f, q01, q23);  // q - 8
-      lo0 = fmaf(q01.x, xc[ch].x, lo0);
-      lo1 = fmaf(q01.y, xc[ch].y, lo1);
-      lo0 = fmaf(q23.x, xc[ch].z, lo0);
-      lo1 = fmaf(q23.y, xc[ch].w, lo1);
+      lo = fma2(q01, mk2(xc[ch].x, xc[ch].y), lo);
+      lo = fma2(q23, mk2(xc[ch].z, xc[ch].w), lo);
       magic4(u.c[ch] & 0xF0F0F0F0u, -8388736.0f, q01, q23);  // 16 (q - 8)
-      hi0 = fmaf(q01.x, xc[ch + 2].x, hi0);
-      hi1 = fmaf(q01.y, xc[ch + 2].y, hi1);
-      hi0 = fmaf(q23.x, xc[ch + 2].z, hi0);
-      hi1 = fmaf(q23.y, xc[ch + 2].w, hi1);
+      hi = fma2(q01, mk2(xc[ch + 2].x, xc[ch + 2].y), hi);
+      hi = fma2(q23, mk2(xc[ch + 2].z, xc[ch + 2].w), hi);
     }
-    return u.d * fmaf(hi0 + hi1, 0.0625f, lo0 + lo1);
+    return u.d * fmaf(hi.x + hi.y, 0.0625f, lo.x + lo.y);
   }
 };
 
@@ -226,18 +220,16 @@ struct Dec<QG_TYPE_Q4_K> {
   // 16 q from the high nibbles in place and scale d*sc by 1/16 (exact)
   QG_DEVICE static float dot1(const U &u, const float4 *xc, float xsum) {
     const uint32_t mask = (u.sh != 0u) ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
-    float s0 = 0.f, s1 = 0.f;
+    f2 s = mk2(0.f, 0.f);
 #pragma unroll
     for (int ch = 0; ch < NCH; ++ch) {
       f2 q01, q23;
       magic4(word(u, ch) & mask, -8388608.0f, q01, q23);
-      s0 = fmaf(q01.x, xc[ch].x, s0);
-      s1 = fmaf(q01.y, xc[ch].y, s1);
-      s0 = fmaf(q23.x, xc[ch].z, s0);
-      s1 = fmaf(q23.y, xc[ch].w, s1);
+      s = fma2(q01, mk2(xc[ch].x, xc[ch].y), s);
+      s = fma2(q23, mk2(xc[ch].z, xc[ch].w), s);
     }
     const float dsc = (u.sh != 0u) ? u.dsc * 0.0625f : u.dsc;
-    return fmaf(dsc, s0 + s1, -u.dm * xsum);
+    return fmaf(dsc, s.x + s.y, -u.dm * xsum);
   }
 };
 
@@ -297,18 +289,16 @@ struct Dec<QG_TYPE_Q6_K> {
     float acc = 0.f;
 #pragma unroll
     for (int qd = 0; qd < 4; ++qd) {
-      float s0 = 0.f, s1 = 0.f;
+      f2 s = mk2(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int ch = 2 * qd + h;
         f2 q01, q23;
         codes(u, ch, q01, q23);
-        s0 = fmaf(q01.x, xc[ch].x, s0);
-        s1 = fmaf(q01.y, xc[ch].y, s1);
-        s0 = fmaf(q23.x, xc[ch].z, s0);
-        s1 = fmaf(q23.y, xc[ch].w, s1);
+        s = fma2(q01, mk2(xc[ch].x, xc[ch].y), s);
+        s = fma2(q23, mk2(xc[ch].z, xc[ch].w), s);
       }
-      acc = fmaf(u.ds[qd], s0 + s1, acc);
+      acc = fmaf(u.ds[qd], s.x + s.y, acc);
     }
     return acc;
   }
