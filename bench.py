@@ -584,8 +584,10 @@ def run_moe(torch, qg, stream, hbm, layers=8, reps=50, warmup=3):
         res[f"T{T}"] = {"us_per_layer": round(us, 2), "unique_experts": round(U, 2),
                         "bytes_per_layer": int(nbytes), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
                         "roofline_us": round(roof_us, 2), "frac_of_roofline": round(roof_us / us, 4),
-                        "launches_per_layer": 4 if T <= 16 else 8, "tokens_per_s": round(T / (us * 1e-6), 1),
-                        "path": "CUDA cores, grouped per expert" if T <= 16 else "tcgen05 grouped per expert (bf16)"}
+                        "launches_per_layer": 1 if T == 1 else 4 if T <= 16 else 8,
+                        "tokens_per_s": round(T / (us * 1e-6), 1),
+                        "path": ("one cooperative launch: router, top-k, gate/up, down + combine" if T == 1 else
+                                 "CUDA cores, grouped per expert" if T <= 16 else "tcgen05 grouped per expert (bf16)")}
         del g
         if qg.device_status() != 0:
             raise RuntimeError("device status set in the MoE benchmark")

@@ -706,11 +706,383 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const __grid_con
 }
 
 // ------------------------------------------------------------------------------------------
+// One token, the whole layer in one cooperative launch
+// ------------------------------------------------------------------------------------------
+// With a single token the layer is four short dependent steps (router, gate/up, down,
+// combine) around ~40 MB of weights, and separate launches spend most of the time on their
+// own start-up and drain.  This kernel runs them as phases of one persistent grid (one CTA
+// per SM, all co-resident: cooperative launch) separated by two grid barriers:
+//   phase 0  router logits, one expert row per CTA (its warps split the row);
+//   barrier
+//   phase 1  every CTA ranks the logits itself (the same picks everywhere), then streams its
+//            share of the {gate i, up i} row pairs of the picked experts and writes
+//            act = silu(g) * u; meanwhile it asks L2 for the down rows it will need next;
+//   barrier
+//   phase 2  every CTA owns a range of hidden rows h: it dots the down rows h of each picked
+//            expert with that expert's act row and adds sum_j w_j dn_j[h] to x[h] in pick
+//            order (the combine needs no separate pass).
+// The grid barrier is an arrival counter in the caller's workspace that only grows (no reset
+// step between calls).  The picks are ranked by the whole CTA at once (a serial warp-level
+// selection costs microseconds of shuffle latency).  Every wait is bounded and reports an
+// expired wait in the status word.
+
+struct OneArgs {
+  const float *xn, *wr;
+  const uint8_t *wg, *wu, *wd;
+  long long stride;  // bytes between expert slots
+  uintptr_t mend_g, mend_u, mend_d;
+  const int32_t *slots;
+  int n_slots, E, k, H, F;
+  int32_t *ids_out;
+  float *wts_out;
+  float *act;        // [k][F]
+  float *x;          // [H], updated in place
+  float *logits;     // [E] (workspace)
+  unsigned long long *bar;  // arrivals of the grid barriers (workspace, 8-byte aligned)
+  long long rbh, rbf;  // bytes of an H-long row (gate, up) and of an F-long row (down)
+  int NS, stage_bytes, gseg, dseg;
+  int hmax;          // most hidden rows of one CTA
+  int early_weights;
+  uint32_t off_x, off_part, off_ring;
+};
+
+QG_DEVICE void prefetch_l2(uintptr_t p, uint32_t n) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
+}
+
+// Grid-wide barrier for a cooperative grid: `bar` counts arrivals and only ever grows.  Every
+// launch adds exactly G per barrier and launches in a stream do not overlap this part (it comes
+// after the wait on the predecessor), so the arrivals of one barrier all return values in
+// [n G, n G + G) for the same n, and the barrier is passed once the count reaches (n + 1) G.
+// Returns false when the wait expired.
+QG_DEVICE bool grid_barrier(unsigned long long *bar, unsigned int nctas, unsigned int *s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's writes are visible before its arrival
+    const unsigned long long v = atomicAdd(bar, 1ull);
+    const unsigned long long target = (v / nctas + 1) * nctas;
+    unsigned int ok = 1u;
+    const uint64_t t0 = global_ns();
+    while (*reinterpret_cast<volatile unsigned long long *>(bar) < target) {
+      if (global_ns() - t0 > QG_WAIT_NS) {
+        ok = 0u;
+        break;
+      }
+    }
+    __threadfence();
+    *s_flag = ok;
+  }
+  __syncthreads();
+  return *s_flag != 0u;
+}
+
+template <int QT, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs a) {
+  using D = Dec<QT>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t *wbar = reinterpret_cast<uint64_t *>(smem);                 // [NW][kMaxNS]
+  int32_t *s_ids = reinterpret_cast<int32_t *>(smem + 512);            // [kMaxK] picks
+  float *s_w = reinterpret_cast<float *>(smem + 640);                  // [kMaxK] weights
+  int32_t *s_slot = reinterpret_cast<int32_t *>(smem + 768);           // [kMaxK] slot, -1: bad id
+  int32_t *s_vz = reinterpret_cast<int32_t *>(smem + 896);             // [kMaxK] valid picks in order
+  float *red = reinterpret_cast<float *>(smem + 1024);                 // [NW] router partials
+  unsigned int *s_misc = reinterpret_cast<unsigned int *>(smem + 1024 + 4 * NW);  // flag, valid count
+  uint8_t *xs = smem + a.off_x;
+  float *part = reinterpret_cast<float *>(smem + a.off_part);          // [hmax][kMaxK]
+  uint8_t *ring = smem + a.off_ring;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = static_cast<int>(gridDim.x);
+  const int H = a.H, F = a.F, k = a.k;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NW * kMaxNS; ++i) mbar_init(&wbar[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // ---- phase 0: router logits of experts blockIdx.x, + G, ..., summed by kRouterWarps warps
+  // in exactly the order of moe_router_kernel, so that the logits (and picks and weights) are
+  // the ones the standalone router gives
+  pdl_wait();
+  bool ok = true;
+  const int H4 = H >> 2;
+  for (int e = blockIdx.x; e < a.E; e += G) {
+    if (warp < kRouterWarps) {
+      const float4 *w4 = reinterpret_cast<const float4 *>(a.wr + static_cast<size_t>(e) * H);
+      const float4 *x4 = reinterpret_cast<const float4 *>(a.xn);
+      float acc = 0.f;
+#pragma unroll 4
+      for (int h = warp * 32 + lane; h < H4; h += kRouterWarps * 32) {
+        const float4 w = __ldg(w4 + h);
+        const float4 xv = __ldg(x4 + h);
+        acc = fmaf(w.x, xv.x, acc);
+        acc = fmaf(w.y, xv.y, acc);
+        acc = fmaf(w.z, xv.z, acc);
+        acc = fmaf(w.w, xv.w, acc);
+      }
+      const float sw = warp_sum(acc);
+      if (lane == 0) red[warp] = sw;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float t = 0.f;
+#pragma unroll
+      for (int w = 0; w < kRouterWarps; ++w) t += red[w];
+      a.logits[e] = t;
+    }
+    __syncthreads();
+  }
+  // the token's activations into shared memory (128-byte swizzled rows) while the grid meets
+  copy_x_row(xs, 0, 0, a.xn, H, threadIdx.x, NW * 32);
+  if (!grid_barrier(a.bar, static_cast<unsigned int>(G), s_misc)) ok = false;
+
+  // ---- phase 1: picks, then the gate/up row pairs.  The k greedy picks of the logits (ties
+  // to the lowest expert id) are the experts of rank < k, rank(e) = #{e' : l[e'] > l[e] or
+  // l[e'] == l[e] and e' < e}; the weights follow in pick order as in topk_token.
+  float *s_l = part;  // the logits (part is free until phase 2)
+  for (int e = threadIdx.x; e < a.E; e += NW * 32) s_l[e] = __ldcg(a.logits + e);
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += NW * 32) {
+    const float le = s_l[e];
+    int rank = 0;
+    for (int f = 0; f < a.E; ++f) {
+      const float lf = s_l[f];
+      rank += (lf > le || (lf == le && f < e)) ? 1 : 0;
+    }
+    if (rank < k) s_ids[rank] = e;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const float lmax = s_l[s_ids[0]];
+    float den = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const float ex = expf(s_l[s_ids[j]] - lmax);
+      den += ex;
+      s_w[j] = ex;
+    }
+    for (int j = 0; j < k; ++j) s_w[j] = s_w[j] / den;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    bool valid = false;
+    int slot = -1;
+    if (lane < k) {
+      const int e = s_ids[lane];
+      valid = e >= 0 && e < a.E;
+      if (valid) {
+        slot = a.slots ? __ldg(a.slots + e) : e;
+        valid = slot >= 0 && slot < a.n_slots;
+      }
+      s_slot[lane] = valid ? slot : -1;
+      if (blockIdx.x == 0) {
+        a.ids_out[lane] = s_ids[lane];
+        a.wts_out[lane] = s_w[lane];
+        if (!valid) moe_status(QG_STATUS_BIT_ID);
+      }
+    }
+    const unsigned int m = __ballot_sync(0xFFFFFFFFu, valid);
+    if (valid) s_vz[__popc(m & ((1u << lane) - 1u))] = lane;
+    if (lane == 0) s_misc[1] = __popc(m);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  const int kv = static_cast<int>(s_misc[1]);
+  // a pick with a bad id has a zero act row
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < k * F; i += NW * 32)
+      if (s_slot[i / F] < 0) a.act[i] = 0.f;
+
+  // hidden rows of phase 2 for this CTA, and their down rows into L2 now
+  const int hA = static_cast<int>(static_cast<long long>(blockIdx.x) * H / G);
+  const int hB = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * H / G);
+  if (warp == NW - 1) {
+    for (int u = lane; u < kv * (hB - hA); u += 32) {
+      const int jv = u / (hB - hA), h = hA + u % (hB - hA);
+      const uintptr_t p = reinterpret_cast<uintptr_t>(a.wd) +
+                          static_cast<uintptr_t>(s_slot[s_vz[jv]]) * static_cast<uintptr_t>(a.stride) +
+                          static_cast<uintptr_t>(h) * static_cast<uintptr_t>(a.rbf);
+      const uintptr_t al = p & ~static_cast<uintptr_t>(15);
+      const uintptr_t want = (p + static_cast<uintptr_t>(a.rbf) + 15) & ~static_cast<uintptr_t>(15);
+      const uintptr_t end = want < a.mend_d ? want : a.mend_d;
+      if (end > al) prefetch_l2(al, static_cast<uint32_t>(end - al));
+    }
+  }
+
+  const uint32_t wo = static_cast<uint32_t>(D::woff(lane));
+  uint32_t xo[D::NCH];
+#pragma unroll
+  for (int ch = 0; ch < D::NCH; ++ch) xo[ch] = x_lane_off<QT>(lane, ch);
+  uint8_t *wring = ring + warp * a.NS * a.stage_bytes;
+  const uint32_t wring_s = smem_u32(wring);
+  const uint32_t xs_s = smem_u32(xs);
+
+  // up to 4 rows against activation row xrow: the dense one-token decode
+  auto dot_rows = [&](const uint32_t (&wrow)[4], int nrows, int K, uint32_t xrow, float (&acc)[4]) {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[r] = 0.f;
+    const int gcount = (K + D::SG - 1) / D::SG;
+    for (int g = 0; g < gcount; ++g) {
+      if (g * D::SG + D::block_first(lane) >= K) break;
+      const uint32_t goff = static_cast<uint32_t>(g * D::GB);
+      const uint32_t xg = xrow + static_cast<uint32_t>(g * (D::SG * 4));
+      float4 xc[D::NCH];
+#pragma unroll
+      for (int ch = 0; ch < D::NCH; ++ch) xc[ch] = lds_f4(xg + xo[ch]);
+      const float aux = D::xaux(xc);
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        if (r < nrows) {
+          typename D::U w = D::load(wrow[r] + goff, lane);
+          acc[r] += D::dot1(w, xc, aux);
+        }
+    }
+  };
+
+  // Streaming of this warp's items through its ring.  Ring positions continue across the
+  // phases, so every slot's mbarrier phase stays in step.  describe(item, r, src, n, mend)
+  // gives row r (< 8) of an item's stage (n = 0: none), stored at r * row_stride in the slot;
+  // consume(item, stage address) computes it.  After an expired wait the warp issues nothing
+  // more and waits for what it has in flight before it exits.
+  int issued = 0, waited = 0, ph_base = 0, ph_n = 0;
+  auto issue_next = [&](auto &&describe, int row_stride) {
+    uintptr_t src = 0, mend = 0;
+    uint32_t n = 0;
+    if (lane < 8) describe(issued - ph_base, lane, src, n, mend);
+    uint8_t *dst = wring + (issued % a.NS) * a.stage_bytes + lane * row_stride;
+    warp_bulk_copies(dst, src, n, mend, &wbar[warp * kMaxNS + issued % a.NS], lane);
+    ++issued;
+  };
+  // begin issues up to `ahead` stages: NS - 1 (the next one is issued before each wait, into
+  // the slot consumed last) or NS (a full ring; each slot is refilled right after it is
+  // consumed)
+  int ph_ahead = 0;
+  auto begin = [&](int n_items, auto &&describe, int row_stride, int ahead) {
+    ph_base = issued;
+    ph_n = n_items;
+    ph_ahead = ahead;
+    while (ok && issued - ph_base < n_items && issued - ph_base < ahead) issue_next(describe, row_stride);
+  };
+  auto finish = [&](auto &&describe, int row_stride, auto &&consume) {
+    const bool full = ph_ahead == a.NS;
+    for (int it = 0; it < ph_n && ok; ++it) {
+      if (!full && issued - ph_base < ph_n) issue_next(describe, row_stride);
+      const int pos = ph_base + it;
+      if (!mbar_wait(&wbar[warp * kMaxNS + pos % a.NS], (pos / a.NS) & 1)) {
+        ok = false;
+        break;
+      }
+      consume(it, wring_s + static_cast<uint32_t>((pos % a.NS) * a.stage_bytes));
+      __syncwarp();  // every lane is done with the slot before it is refilled
+      ++waited;
+      if (full && issued - ph_base < ph_n) issue_next(describe, row_stride);
+    }
+  };
+
+  // gate/up: row pairs (pick jv, row i), contiguous balanced ranges per CTA; stage row 0 is the
+  // gate row, row 1 the up row
+  {
+    const long long nb = static_cast<long long>(kv) * F;
+    const long long bA = static_cast<long long>(blockIdx.x) * nb / G, bB = static_cast<long long>(blockIdx.x + 1) * nb / G;
+    const int nrb = static_cast<int>(bB - bA);
+    const int n_items = warp < nrb ? (nrb - warp + NW - 1) / NW : 0;
+    auto pair_of = [&](int item, int &jv, int &i) {
+      const long long b = bA + warp + static_cast<long long>(item) * NW;
+      jv = static_cast<int>(b / F);
+      i = static_cast<int>(b - static_cast<long long>(jv) * F);
+    };
+    auto row_src = [&](int jv, int i, int r) {
+      return reinterpret_cast<uintptr_t>(r == 0 ? a.wg : a.wu) +
+             static_cast<uintptr_t>(s_slot[s_vz[jv]]) * static_cast<uintptr_t>(a.stride) +
+             static_cast<uintptr_t>(i) * static_cast<uintptr_t>(a.rbh);
+    };
+    auto describe = [&](int item, int r, uintptr_t &src, uint32_t &n, uintptr_t &mend) {
+      if (r > 1) return;
+      int jv, i;
+      pair_of(item, jv, i);
+      src = row_src(jv, i, r);
+      n = static_cast<uint32_t>(a.rbh);
+      mend = r == 0 ? a.mend_g : a.mend_u;
+    };
+    begin(n_items, describe, a.gseg, a.NS - 1);
+    finish(describe, a.gseg, [&](int item, uint32_t st) {
+      int jv, i;
+      pair_of(item, jv, i);
+      const uint32_t wrow[4] = {st + (static_cast<uint32_t>(row_src(jv, i, 0)) & 15u) + wo,
+                                st + static_cast<uint32_t>(a.gseg) + (static_cast<uint32_t>(row_src(jv, i, 1)) & 15u) + wo,
+                                0u, 0u};
+      float acc[4];
+      dot_rows(wrow, 2, H, xs_s, acc);
+      const float gsum = warp_sum(acc[0]), usum = warp_sum(acc[1]);
+      if (lane == 0) a.act[static_cast<size_t>(s_vz[jv]) * F + i] = silu_mul(gsum, usum);
+    });
+  }
+
+  // down: items (pick jv, 4 consecutive hidden rows of this CTA), one copy of the rows (they
+  // are contiguous); their first stages are requested before the barrier (the rows are known)
+  const int nh = hB - hA, nqd = (nh + 3) / 4;
+  const int n2 = warp < kv * nqd ? (kv * nqd - warp + NW - 1) / NW : 0;
+  auto item2 = [&](int item, int &jv, int &h0, int &nr) {
+    const int u = warp + item * NW;
+    jv = u / nqd;
+    h0 = 4 * (u - jv * nqd);
+    nr = min(4, nh - h0);
+  };
+  auto down_src = [&](int jv, int hl) {
+    return reinterpret_cast<uintptr_t>(a.wd) + static_cast<uintptr_t>(s_slot[s_vz[jv]]) * static_cast<uintptr_t>(a.stride) +
+           static_cast<uintptr_t>(hA + hl) * static_cast<uintptr_t>(a.rbf);
+  };
+  auto describe2 = [&](int item, int r, uintptr_t &src, uint32_t &n, uintptr_t &mend) {
+    if (r != 0) return;
+    int jv, h0, nr;
+    item2(item, jv, h0, nr);
+    src = down_src(jv, h0);
+    n = static_cast<uint32_t>(nr) * static_cast<uint32_t>(a.rbf);
+    mend = a.mend_d;
+  };
+  begin(n2, describe2, a.dseg, a.NS);
+  if (!grid_barrier(a.bar, static_cast<unsigned int>(G), s_misc)) ok = false;
+  pdl_launch_dependents();
+
+  // ---- phase 2: the act rows of the valid picks into shared memory, the down dots, and the
+  // combine for this CTA's hidden rows
+  const int xrow_f = ((F + D::SG - 1) / D::SG) * D::SG * 4;  // bytes per act row in shared memory
+  for (int jv = 0; jv < kv; ++jv) copy_x_row(xs, jv, xrow_f, a.act + static_cast<size_t>(s_vz[jv]) * F, F, threadIdx.x, NW * 32);
+  cp_async_wait_all();
+  __syncthreads();
+  finish(describe2, a.dseg, [&](int item, uint32_t st) {
+    int jv, h0, nr;
+    item2(item, jv, h0, nr);
+    const uint32_t r0 = st + (static_cast<uint32_t>(down_src(jv, h0)) & 15u) + wo;
+    const uint32_t rb = static_cast<uint32_t>(a.rbf);
+    const uint32_t wrow[4] = {r0, r0 + rb, r0 + 2u * rb, r0 + 3u * rb};
+    float acc[4];
+    dot_rows(wrow, nr, F, xs_s + static_cast<uint32_t>(jv * xrow_f), acc);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float d = warp_sum(acc[r]);
+      if (lane == 0 && r < nr) part[(h0 + r) * kMaxK + jv] = d;
+    }
+  });
+  __syncthreads();
+  for (int hl = threadIdx.x; hl < nh; hl += NW * 32) {
+    float sum = 0.f;
+    for (int jv = 0; jv < kv; ++jv) sum = fmaf(s_w[s_vz[jv]], part[hl * kMaxK + jv], sum);
+    if (ok) a.x[hA + hl] += sum;
+  }
+  if (!ok) {
+    if (lane == 0) moe_status(QG_STATUS_BIT_TIMEOUT);
+    if (lane == 0)
+      for (int it = waited; it < issued; ++it) mbar_wait(&wbar[warp * kMaxNS + (it % a.NS)], (it / a.NS) & 1);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
 // Host side
 // ------------------------------------------------------------------------------------------
 
 struct WsLayout {
-  size_t logits, ticket, dn, tc, total;
+  size_t logits, ticket, bar, dn, tc, total;
 };
 
 inline size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -719,7 +1091,10 @@ WsLayout ws_layout(int T, int k, int E, int H, int F = 0) {
   WsLayout w;
   w.logits = 0;
   w.ticket = up256(static_cast<size_t>(T) * E * 4);
-  w.dn = w.ticket + up256(static_cast<size_t>((T + kRouterTB - 1) / kRouterTB) * 4);
+  // router tickets, then the two words of the one-token layer's grid barrier
+  const size_t tickets = static_cast<size_t>((T + kRouterTB - 1) / kRouterTB) * 4;
+  w.bar = w.ticket + ((tickets + 15) & ~static_cast<size_t>(15));
+  w.dn = w.ticket + up256(((tickets + 15) & ~static_cast<size_t>(15)) + 16);
   w.tc = w.dn + up256(static_cast<size_t>(T) * k * H * 4);
   w.total = w.tc;
   // grouped tensor-core path (more than 16 tokens): plan, grouped bf16 rows
@@ -858,6 +1233,98 @@ uintptr_t tensor_mend(const void *base, long long stride, int n_slots, long long
   const uintptr_t end = reinterpret_cast<uintptr_t>(base) + static_cast<uintptr_t>(stride) * (n_slots - 1) +
                         static_cast<uintptr_t>(mat_bytes);
   return end & ~static_cast<uintptr_t>(15);
+}
+
+// The one-token layer in one cooperative launch; QG_EUNSUPPORTED (nothing launched) when the
+// shapes do not fit its shared-memory plan or the grid cannot be co-resident.
+template <int QT>
+qg_status launch_one_token(OneArgs a, cudaStream_t s) {
+  using D = Dec<QT>;
+  constexpr int NW = 16;
+  const qg::DeviceInfo &dev = qg::device_info();
+  if (!dev.ok) return QG_ECUDA;
+  if (a.k > kMaxK) return QG_EUNSUPPORTED;
+  const int G = dev.sms;
+  const uint32_t hdr = 2048;
+  const long long xrow_h = static_cast<long long>((a.H + D::SG - 1) / D::SG) * D::SG * 4;
+  const long long xrow_f = static_cast<long long>((a.F + D::SG - 1) / D::SG) * D::SG * 4;
+  const long long xbytes = ((std::max(xrow_h, a.k * xrow_f) + 1023) / 1024) * 1024;
+  a.hmax = (a.H + G - 1) / G;
+  // per-row pick dots of phase 2; the logits for the ranking before that
+  const long long part = ((std::max<long long>(static_cast<long long>(a.hmax) * kMaxK, kMaxE) * 4 + 1023) / 1024) * 1024;
+  a.gseg = static_cast<int>(((a.rbh + 15) & ~15LL) + 32);
+  a.dseg = static_cast<int>(((a.rbf + 15) & ~15LL) + 32);
+  const long long stage = std::max<long long>(2LL * a.gseg, ((4 * a.rbf + 15) & ~15LL) + 32);
+  const long long ring = dev.smem_optin - 1024 - hdr - xbytes - part;
+  const int NS = ring > 0 ? static_cast<int>(std::min<long long>(kMaxNS, ring / (NW * stage))) : 0;
+  if (NS < 2) return QG_EUNSUPPORTED;
+  a.NS = NS;
+  a.stage_bytes = static_cast<int>(stage);
+  a.off_x = hdr;
+  a.off_part = static_cast<uint32_t>(hdr + xbytes);
+  a.off_ring = static_cast<uint32_t>(hdr + xbytes + part);
+  const uint32_t smem = a.off_ring + static_cast<uint32_t>(NW * NS * stage) + 1024;
+  auto kern = moe_one_token_kernel<QT, NW>;
+  if (!qg::set_smem_attr(reinterpret_cast<const void *>(kern), smem)) return QG_ECUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem) != cudaSuccess || per_sm < 1)
+    return QG_EUNSUPPORTED;
+  a.early_weights = qg::static_weights() ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, kern, a) != cudaSuccess) return QG_ECUDA;
+  return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+}
+
+qg_status one_token_layer(int type, const float *xn, const float *wr, const void *w_gate, const void *w_up,
+                          const void *w_down, int64_t stride, const int32_t *slots, int n_slots, int H, int F, int E,
+                          int k, int32_t *ids, float *weights, float *act, float *x_inout, void *ws, cudaStream_t s) {
+  int qk = 0, bb = 0;
+  qg_block_shape(type, &qk, &bb);
+  if (!qg::aligned16(xn) || !qg::aligned16(wr) || !qg::aligned16(act) || !qg::aligned16(ws)) return QG_EUNSUPPORTED;
+  OneArgs a{};
+  a.xn = xn;
+  a.wr = wr;
+  a.wg = static_cast<const uint8_t *>(w_gate);
+  a.wu = static_cast<const uint8_t *>(w_up);
+  a.wd = static_cast<const uint8_t *>(w_down);
+  a.stride = stride;
+  const long long mat_gu = static_cast<long long>(F) * (H / qk) * bb, mat_d = static_cast<long long>(H) * (F / qk) * bb;
+  a.mend_g = tensor_mend(w_gate, stride, n_slots, mat_gu);
+  a.mend_u = tensor_mend(w_up, stride, n_slots, mat_gu);
+  a.mend_d = tensor_mend(w_down, stride, n_slots, mat_d);
+  a.slots = slots;
+  a.n_slots = n_slots;
+  a.E = E;
+  a.k = k;
+  a.H = H;
+  a.F = F;
+  a.ids_out = ids;
+  a.wts_out = weights;
+  a.act = act;
+  a.x = x_inout;
+  const WsLayout L = ws_layout(1, k, E, H, F);
+  a.logits = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + L.logits);
+  a.bar = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(ws) + L.bar);
+  a.rbh = static_cast<long long>(H / qk) * bb;
+  a.rbf = static_cast<long long>(F / qk) * bb;
+  switch (type) {
+    case QG_TYPE_Q8_0: return launch_one_token<QG_TYPE_Q8_0>(a, s);
+    case QG_TYPE_Q4_0: return launch_one_token<QG_TYPE_Q4_0>(a, s);
+    case QG_TYPE_Q4_K: return launch_one_token<QG_TYPE_Q4_K>(a, s);
+    case QG_TYPE_Q6_K: return launch_one_token<QG_TYPE_Q6_K>(a, s);
+    default: return QG_EUNSUPPORTED;
+  }
 }
 
 qg_status expert_checks(int type, int T, int k, int E, int H, int F, int n_slots, long long stride) {
@@ -1066,6 +1533,12 @@ qg_status moe_layer(int type, const float *xn, const float *wr, const void *w_ga
     if (r != QG_OK) return r;
     return combine_impl(type, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout, 1,
                         ws, ws_bytes, s);
+  }
+  // one token: the whole layer in one cooperative launch when it fits
+  if (T == 1) {
+    r = one_token_layer(type, xn, wr, w_gate, w_up, w_down, expert_stride, slots, n_slots, H, F, E, k, ids, weights,
+                        act, x_inout, ws, s);
+    if (r != QG_EUNSUPPORTED) return r;
   }
   // router logits into the workspace; the gate/up kernel ranks them (every CTA needs the
   // picks for its plan anyway) and stores ids and weights for the combine
