@@ -59,7 +59,7 @@ def parse():
                    help="static: the weights are immutable parameters, so each GEMV may start streaming "
                         "them before its predecessor ends (qg_set_static_weights); ordered: every launch "
                         "waits for its predecessor before it reads anything")
-    p.add_argument("--sections", choices=["main", "all", "gemm", "moe", "kquant", "proj"], default="all",
+    p.add_argument("--sections", choices=["main", "all", "gemm", "moe", "moe1", "kquant", "proj"], default="all",
                    help="main: the headline line only; all: plus the detail object; gemm / moe / kquant / "
                         "proj: only that detail section, printed as its own JSON line (for profiling runs)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -342,6 +342,8 @@ def run_section(args):
         res = run_gemm(torch, qg, stream, reps=args.steps, warmup=args.warmup)
     elif args.sections == "moe":
         res = run_moe(torch, qg, stream, hbm, reps=args.steps, warmup=args.warmup)
+    elif args.sections == "moe1":  # one expert pool, one token: a small case for profiling
+        res = run_moe(torch, qg, stream, hbm, layers=1, reps=args.steps, warmup=args.warmup, Ts=(1,))
     elif args.sections == "kquant":
         res = run_kquant(torch, qg, stream, hbm, reps=args.steps, warmup=args.warmup)
     else:
@@ -548,7 +550,7 @@ def run_gemm(torch, qg, stream, reps=10, warmup=3):
     return res
 
 
-def run_moe(torch, qg, stream, hbm, layers=8, reps=50, warmup=3):
+def run_moe(torch, qg, stream, hbm, layers=8, reps=50, warmup=3, Ts=(1, 8, 512)):
     """Qwen3-30B-A3B-shaped MoE layer in Q8_0 (H 2048, F 768, 128 experts, top-8): one
     moe_layer call per layer, each layer with its own expert pool and its own input tokens,
     rotating over `layers` pools (8 x 641 MB, far above L2)."""
@@ -559,7 +561,7 @@ def run_moe(torch, qg, stream, hbm, layers=8, reps=50, warmup=3):
     pools = [base] + [base.clone() for _ in range(layers - 1)]
     wr = [torch.from_numpy(gs.router_weights(E, H, seed=l)).to(dev) for l in range(layers)]
     res = {}
-    for T in (1, 8, 512):
+    for T in Ts:
         xn = [torch.from_numpy(gs.activations(T, H, seed=l, stream=40)).to(dev) for l in range(layers)]
         x = torch.from_numpy(gs.activations(T, H, seed=0, stream=41)).to(dev)
         ids = torch.zeros((layers, T, k), dtype=torch.int32, device=dev)
