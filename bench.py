@@ -59,7 +59,7 @@ def parse():
                    help="static: the weights are immutable parameters, so each GEMV may start streaming "
                         "them before its predecessor ends (qg_set_static_weights); ordered: every launch "
                         "waits for its predecessor before it reads anything")
-    p.add_argument("--sections", choices=["main", "all", "gemm", "moe", "moe1", "kquant", "proj"], default="all",
+    p.add_argument("--sections", choices=["main", "all", "gemm", "moe", "moe1", "moe8", "kquant", "proj"], default="all",
                    help="main: the headline line only; all: plus the detail object; gemm / moe / kquant / "
                         "proj: only that detail section, printed as its own JSON line (for profiling runs)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -344,6 +344,8 @@ def run_section(args):
         res = run_moe(torch, qg, stream, hbm, reps=args.steps, warmup=args.warmup)
     elif args.sections == "moe1":  # one expert pool, one token: a small case for profiling
         res = run_moe(torch, qg, stream, hbm, layers=1, reps=args.steps, warmup=args.warmup, Ts=(1,))
+    elif args.sections == "moe8":  # one expert pool, eight tokens: a small case for profiling
+        res = run_moe(torch, qg, stream, hbm, layers=1, reps=args.steps, warmup=args.warmup, Ts=(8,))
     elif args.sections == "kquant":
         res = run_kquant(torch, qg, stream, hbm, reps=args.steps, warmup=args.warmup)
     else:
