@@ -365,10 +365,24 @@ __global__ void qgemm_prep_kernel(const float4 *__restrict__ x, uint2 *__restric
   pdl_wait();
   pdl_launch_dependents();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
-    const float4 v = __ldg(x + i);
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-    xb[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+  // eight independent loads in flight per thread, then their conversions and stores: one
+  // memory round trip per eight elements instead of one each
+  constexpr int U = 8;
+  for (long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n4; i0 += U * stride) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long i = i0 + u * stride;
+      v[u] = i < n4 ? __ldg(x + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long i = i0 + u * stride;
+      if (i < n4) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(v[u].x, v[u].y), hi = __floats2bfloat162_rn(v[u].z, v[u].w);
+        xb[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo), *reinterpret_cast<const uint32_t *>(&hi));
+      }
+    }
   }
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < ncnt; i += stride)
     cnt[i] = 0u;
@@ -441,7 +455,7 @@ qg_status gemm_tc(const void *w, const float *x, float *y, int64_t M, int64_t N,
       return QG_ECUDA;
   }
   const long long n4 = T * N / 4;
-  const int pb = static_cast<int>(std::min<long long>(4LL * dev.sms, (n4 + 255) / 256));
+  const int pb = static_cast<int>(std::min<long long>(4LL * dev.sms, (n4 + 8 * 256 - 1) / (8 * 256)));
   if (qg::launch_pdl(qgemm_prep_kernel, dim3(std::max(pb, 1)), dim3(256), 0, s, reinterpret_cast<const float4 *>(x),
                      reinterpret_cast<uint2 *>(xb), n4, cnt, p.n_mt * p.n_tt) != cudaSuccess)
     return QG_ECUDA;

@@ -204,6 +204,8 @@ struct PlanSmem {
   int *s_id, *s_pairs, *u_slot, *u_first, *u_cnt, *s_cnt, *s_start, *s_ustart, *s_kv;
   int32_t *tk_ids;  // fused top-k results [T][k]
   float *tk_w;
+  float *tk_lg;     // the router logits being ranked [T][E] (fused top-k, several tokens; lives in
+                    // the activation buffer, which is filled only after the plan)
 };
 
 QG_DEVICE PlanSmem plan_layout(uint8_t *base, int P, int T) {
@@ -230,6 +232,7 @@ QG_DEVICE PlanSmem plan_layout(uint8_t *base, int P, int T) {
   p.tk_ids = q;
   q += P;
   p.tk_w = reinterpret_cast<float *>(q);
+  p.tk_lg = nullptr;  // set by the kernel: the activation buffer, still unused while the plan is built
   return p;
 }
 
@@ -243,8 +246,36 @@ QG_DEVICE int build_plan(const MoeArgs &a, int TT, const PlanSmem &p) {
   const int P = a.T * a.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (a.fuse_topk) {
-    for (int t = warp; t < a.T; t += NW)
-      topk_token(a.logits + static_cast<size_t>(t) * a.E, a.E, a.k, lane, p.tk_ids + t * a.k, p.tk_w + t * a.k);
+    // the k greedy picks of each token (ties to the lowest expert id) are the experts of rank
+    // < k, rank(e) = #{e' : l[e'] > l[e] or l[e'] == l[e] and e' < e}: one thread per (token,
+    // expert) instead of a warp-serial selection; the weights follow in pick order as in
+    // topk_token, so picks and weights equal the standalone router's
+    const int TE = a.T * a.E;
+    for (int i = tid; i < TE; i += NW * 32) p.tk_lg[i] = __ldcg(a.logits + i);
+    __syncthreads();
+    for (int i = tid; i < TE; i += NW * 32) {
+      const int t = i / a.E, e = i - t * a.E;
+      const float *lt = p.tk_lg + t * a.E;
+      const float le = lt[e];
+      int rank = 0;
+      for (int f = 0; f < a.E; ++f) {
+        const float lf = lt[f];
+        rank += (lf > le || (lf == le && f < e)) ? 1 : 0;
+      }
+      if (rank < a.k) p.tk_ids[t * a.k + rank] = e;
+    }
+    __syncthreads();
+    for (int t = tid; t < a.T; t += NW * 32) {
+      const float *lt = p.tk_lg + t * a.E;
+      const float lmax = lt[p.tk_ids[t * a.k]];
+      float den = 0.f;
+      for (int j = 0; j < a.k; ++j) {
+        const float ex = expf(lt[p.tk_ids[t * a.k + j]] - lmax);
+        den += ex;
+        p.tk_w[t * a.k + j] = ex;
+      }
+      for (int j = 0; j < a.k; ++j) p.tk_w[t * a.k + j] = p.tk_w[t * a.k + j] / den;
+    }
     __syncthreads();
     if (blockIdx.x == 0)
       for (int z = tid; z < P; z += NW * 32) {
@@ -413,8 +444,9 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const __grid_con
   uint64_t *wbar = reinterpret_cast<uint64_t *>(smem);  // [NW][kMaxNS]
   uint64_t *xbar = wbar + NW * kMaxNS;                   // one token: activation rows by TMA
   const int P = a.T * a.k;
-  const PlanSmem pl = plan_layout(smem + a.off_plan, P, a.T);
+  PlanSmem pl = plan_layout(smem + a.off_plan, P, a.T);
   uint8_t *xs = smem + a.off_x;
+  pl.tk_lg = reinterpret_cast<float *>(xs);
   uint8_t *ring = smem + a.off_ring;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
