@@ -236,7 +236,7 @@ class ClockSampler:
 
 def profiled_traffic():
     """DRAM bytes per launch of the headline kernel from the committed ncu summary, when that
-    summary was taken on the current kernel sources (same hash); else None."""
+    summary was taken on the current sources of that kernel (same hash); else None."""
     path = os.path.join(ROOT, "profiles", "qgemv_q8_0_qwen3_4b_decode_t1.md")
     if not os.path.exists(path):
         return None
@@ -251,12 +251,14 @@ def profiled_traffic():
 
 
 def kernel_source_hash():
-    d = os.path.join(ROOT, "gguf_block_dequant_gb300", "csrc")
+    """Hash of the headline kernel's sources: its translation unit and the headers it includes."""
+    csrc = os.path.join(ROOT, "gguf_block_dequant_gb300", "csrc")
+    files = [os.path.join(csrc, f) for f in ("qg_gemv.cu", "qg_decode.cuh", "qg_common.cuh", "qg_pipe.cuh", "qg_host.h")]
+    files.append(os.path.join(ROOT, "include", "ggufdq.h"))
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(f.encode())
-            h.update(open(os.path.join(d, f), "rb").read())
+    for path in files:
+        h.update(os.path.basename(path).encode())
+        h.update(open(path, "rb").read())
     return h.hexdigest()[:16]
 
 
