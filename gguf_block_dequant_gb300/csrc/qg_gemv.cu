@@ -102,7 +102,7 @@ __host__ __device__ constexpr int rows_per_block() {
 }
 
 template <int QT, int TT, int NW>
-__global__ void __launch_bounds__(NW * 32, (TT == 1) ? 2 : 1) qgemv_kernel(const __grid_constant__ CUtensorMap xmap, const GemvArgs a) {
+__global__ void __launch_bounds__(NW * 32, (TT == 1 && NW == 8) ? 2 : 1) qgemv_kernel(const __grid_constant__ CUtensorMap xmap, const GemvArgs a) {
   using D = Dec<QT>;
   constexpr int RR = rows_per_block<TT>();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -381,14 +381,10 @@ __global__ void __launch_bounds__(NW * 32, (TT == 1) ? 2 : 1) qgemv_kernel(const
 // Host side
 // ------------------------------------------------------------------------------------------
 
-template <int QT, int TT>
-qg_status launch_t(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
-                   int T, cudaStream_t stream) {
+template <int QT, int TT, int NW, int CPS>
+qg_status launch_cfg(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
+                     int T, cudaStream_t stream) {
   using D = Dec<QT>;
-  // One token: CTAs of 8 warps, two per SM (half the shared memory each), so that the next
-  // kernel's CTAs can already sit on an SM while this kernel's last CTAs drain.
-  constexpr int NW = 8;
-  constexpr int CPS = (TT == 1) ? 2 : 1;  // CTAs per SM
   const qg::DeviceInfo &dev = qg::device_info();
   if (!dev.ok) return QG_ECUDA;
   const int ngroups = static_cast<int>((N + D::SG - 1) / D::SG);
@@ -523,6 +519,27 @@ qg_status launch_t(int nmat, const void *const *w, const float *x, float *const 
   a.early_weights = qg::static_weights() ? 1 : 0;
   if (qg::launch_pdl(kern, dim3(grid), dim3(NW * 32), smem, stream, map, a) != cudaSuccess) return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+}
+
+// CTA shape per launch.  One token: CTAs of 8 warps, two per SM (half the shared memory each),
+// so that the next kernel's CTAs can already sit on an SM while this kernel's last CTAs drain.
+// Q4_K rows whose activations would not stay resident in half an SM (above 56 KB) take one
+// 16-warp CTA per SM instead, which holds them once beside a large ring (measured: 36 -> 27 us
+// on 5120 x 17408; the same shape is slower for Q6_K and for the Q8_0 rows of 9728).  Several
+// tokens: one 8-warp CTA per SM.
+template <int QT, int TT>
+qg_status launch_t(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
+                   int T, cudaStream_t stream) {
+  if constexpr (TT == 1) {
+    if constexpr (QT == QG_TYPE_Q4_K) {
+      using D = Dec<QT>;
+      const long long xres = (N + D::SG - 1) / D::SG * D::SG * 4;
+      if (xres > 56 * 1024) return launch_cfg<QT, 1, 16, 1>(nmat, w, x, y, Ms, N, T, stream);
+    }
+    return launch_cfg<QT, 1, 8, 2>(nmat, w, x, y, Ms, N, T, stream);
+  } else {
+    return launch_cfg<QT, TT, 8, 1>(nmat, w, x, y, Ms, N, T, stream);
+  }
 }
 
 template <int QT>
