@@ -313,3 +313,71 @@ QG_DEVICE uint32_t x_lane_off(int lane, int ch) {
   const int R = D::xrow(lane, ch);
   return 128u * static_cast<uint32_t>(R) + 16u * static_cast<uint32_t>(D::xunit(lane, ch) ^ (R & 7));
 }
+
+// A lane's unit addresses prepared once per row for the one-token loop.  Consecutive groups
+// of a row are GB bytes apart and GB is a multiple of 4 for every type, so the alignment of
+// the lane's unit inside its 32-bit words is the same in every group of the row: the
+// word-aligned base and the funnel-shift amount are computed once, and a group costs one add
+// per address.
+template <int QT>
+struct RowPrep {
+  uint32_t blk;
+  QG_DEVICE void init(uint32_t b, int) { blk = b; }
+  QG_DEVICE typename Dec<QT>::U load(uint32_t goff, int lane) const { return Dec<QT>::load(blk + goff, lane); }
+};
+
+template <>
+struct RowPrep<QG_TYPE_Q8_0> {
+  static_assert(Dec<QG_TYPE_Q8_0>::GB % 4 == 0, "groups keep the word alignment");
+  uint32_t dp, cw, sh;  // the block's scale, the first word holding the lane's codes, shift
+  QG_DEVICE void init(uint32_t b, int lane) {
+    const uint32_t a = b + 2u + 16u * static_cast<uint32_t>(lane & 1);
+    dp = b;
+    cw = a & ~3u;
+    sh = (a & 3u) * 8u;
+  }
+  QG_DEVICE Dec<QG_TYPE_Q8_0>::U load(uint32_t goff, int) const {
+    Dec<QG_TYPE_Q8_0>::U u;
+    uint32_t d16;
+    QG_LDS16(dp + goff, 0, d16);
+    u.d = h2f(d16);
+    const uint32_t b = cw + goff;
+    uint32_t w0, w1, w2, w3, w4;
+    QG_LDS32(b, 0, w0);
+    QG_LDS32(b, 4, w1);
+    QG_LDS32(b, 8, w2);
+    QG_LDS32(b, 12, w3);
+    QG_LDS32(b, 16, w4);
+    u.c[0] = __funnelshift_r(w0, w1, sh);
+    u.c[1] = __funnelshift_r(w1, w2, sh);
+    u.c[2] = __funnelshift_r(w2, w3, sh);
+    u.c[3] = __funnelshift_r(w3, w4, sh);
+    return u;
+  }
+};
+
+template <>
+struct RowPrep<QG_TYPE_Q4_0> {
+  static_assert(Dec<QG_TYPE_Q4_0>::GB % 4 == 0, "groups keep the word alignment");
+  uint32_t dp, cw, sh;
+  QG_DEVICE void init(uint32_t b, int lane) {
+    const uint32_t a = b + 2u + 8u * static_cast<uint32_t>(lane & 1);
+    dp = b;
+    cw = a & ~3u;
+    sh = (a & 3u) * 8u;
+  }
+  QG_DEVICE Dec<QG_TYPE_Q4_0>::U load(uint32_t goff, int) const {
+    Dec<QG_TYPE_Q4_0>::U u;
+    uint32_t d16;
+    QG_LDS16(dp + goff, 0, d16);
+    u.d = h2f(d16);
+    const uint32_t b = cw + goff;
+    uint32_t w0, w1, w2;
+    QG_LDS32(b, 0, w0);
+    QG_LDS32(b, 4, w1);
+    QG_LDS32(b, 8, w2);
+    u.c[0] = __funnelshift_r(w0, w1, sh);
+    u.c[1] = __funnelshift_r(w1, w2, sh);
+    return u;
+  }
+};

@@ -273,8 +273,13 @@ __global__ void __launch_bounds__(NW * 32, (TT == 1 && NW == 8) ? 2 : 1) qgemv_k
       // activation base of this chunk's first group
       const uint32_t xg0 = smem_u32(xs) + (a.mode == 0 ? static_cast<uint32_t>(cc.c * gpc * (D::SG * 4))
                                                         : static_cast<uint32_t>(cc.c & 1) * a.xbuf_bytes);
-      for (int g = 0; g < gcount; ++g) {
-        if (g * D::SG + D::block_first(lane) >= kel) break;
+      // one token: the groups in which every lane's unit is in range, then the last, partial
+      // group with a per-lane check (several tokens keep the per-group check)
+      const int gfull = kel / D::SG;
+      RowPrep<QT> rp[RR];
+#pragma unroll
+      for (int r = 0; r < RR; ++r) rp[r].init(wrow[r], lane);
+      auto group = [&](int g) {
         const uint32_t goff = static_cast<uint32_t>(g * D::GB);
         const uint32_t xg = xg0 + static_cast<uint32_t>(g * (D::SG * 4));
         if constexpr (TT == 1) {
@@ -284,7 +289,7 @@ __global__ void __launch_bounds__(NW * 32, (TT == 1 && NW == 8) ? 2 : 1) qgemv_k
           const float aux = D::xaux(xc);
           typename D::U u[RR];
 #pragma unroll
-          for (int r = 0; r < RR; ++r) u[r] = D::load(wrow[r] + goff, lane);
+          for (int r = 0; r < RR; ++r) u[r] = rp[r].load(goff, lane);
 #pragma unroll
           for (int r = 0; r < RR; ++r) acc1[r] += D::dot1(u[r], xc, aux);
         } else {
@@ -309,6 +314,15 @@ __global__ void __launch_bounds__(NW * 32, (TT == 1 && NW == 8) ? 2 : 1) qgemv_k
               }
             }
           }
+        }
+      };
+      if constexpr (TT == 1) {
+        for (int g = 0; g < gfull; ++g) group(g);
+        if (gfull < gcount && gfull * D::SG + D::block_first(lane) < kel) group(gfull);
+      } else {
+        for (int g = 0; g < gcount; ++g) {
+          if (g * D::SG + D::block_first(lane) >= kel) break;
+          group(g);
         }
       }
     }

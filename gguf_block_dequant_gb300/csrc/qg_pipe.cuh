@@ -1,6 +1,6 @@
 // qg_pipe.cuh -- pieces of the warp-autonomous streaming pipeline shared by the GEMV and
-// MoE kernels: activation tensor copies, unaligned bulk-copy sizing, the one-token row-block
-// inner loop, and the host-side tensor-map encoder.
+// MoE kernels: activation tensor copies, unaligned bulk-copy sizing and the host-side
+// tensor-map encoder.
 #pragma once
 
 #include <cuda.h>
@@ -58,31 +58,6 @@ QG_DEVICE void warp_bulk_copies(uint8_t *dst, uintptr_t src, uint32_t n, uintptr
   if (nb) {
     fence_proxy_async_smem();  // the slot's previous bytes were read through the generic proxy
     bulk_g2s(dst, reinterpret_cast<const void *>(src & ~static_cast<uintptr_t>(15)), nb, bar);
-  }
-}
-
-// One-token inner loop over the groups of a stage: 4 rows (shared-memory unit addresses
-// wrow[r], already offset by the lane's unit) against the activation chunk whose first
-// group starts at shared address xg0; xo[ch] are the lane's swizzled chunk offsets.
-// Accumulates into acc[4].  kel is the number of valid elements in this chunk.
-template <int QT>
-QG_DEVICE void rows_dot1(const uint32_t (&wrow)[4], uint32_t xg0, const uint32_t (&xo)[Dec<QT>::NCH], int kel, int lane,
-                         float (&acc)[4]) {
-  using D = Dec<QT>;
-  const int gcount = (kel + D::SG - 1) / D::SG;
-  for (int g = 0; g < gcount; ++g) {
-    if (g * D::SG + D::block_first(lane) >= kel) break;
-    const uint32_t goff = static_cast<uint32_t>(g * D::GB);
-    const uint32_t xg = xg0 + static_cast<uint32_t>(g * (D::SG * 4));
-    float4 xc[D::NCH];
-#pragma unroll
-    for (int ch = 0; ch < D::NCH; ++ch) xc[ch] = lds_f4(xg + xo[ch]);
-    const float aux = D::xaux(xc);
-    typename D::U u[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) u[r] = D::load(wrow[r] + goff, lane);
-#pragma unroll
-    for (int r = 0; r < 4; ++r) acc[r] += D::dot1(u[r], xc, aux);
   }
 }
 
