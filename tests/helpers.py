@@ -1,7 +1,7 @@
 """Shared helpers for the parity tests (GPU path vs the CPU oracle)."""
 import numpy as np
 
-# spec bar for every GEMV / MoE output element: |gpu - oracle| <= 1e-5 * B + 1e-6,
+# tolerance for every GEMV / MoE output element: |gpu - oracle| <= 1e-5 * B + 1e-6,
 # with B the sum of |products| that form the element
 REL = 1e-5
 ABS = 1e-6
