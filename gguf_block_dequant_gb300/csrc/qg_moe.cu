@@ -492,10 +492,28 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const __grid_con
   // Stage of one item: whole rows (seg_slot == 0; one copy of the block's down rows, or one
   // copy of its gate rows and one of its up rows) or one copy per row segment.
   const bool whole = a.seg_slot == 0;
-  auto issue = [&](int item, int s) {
-    const int i = item / a.nchunks, c = item - i * a.nchunks;
-    const long long rb = rbA + warp + static_cast<long long>(i) * NW;
-    const int u = static_cast<int>(rb / a.nblk), p = static_cast<int>(rb - static_cast<long long>(u) * a.nblk);
+  // Item cursor: chunk c of row block p of unit u, advanced without divisions (a warp's row
+  // blocks are NW apart, so u and p move by whole strides).
+  struct ItemCur {
+    int c, u, p;
+  };
+  auto cur_first = [&]() {
+    const long long rb = rbA + warp;
+    const int u0 = static_cast<int>(rb / a.nblk);
+    return ItemCur{0, u0, static_cast<int>(rb - static_cast<long long>(u0) * a.nblk)};
+  };
+  auto cur_next = [&](ItemCur &q) {
+    if (++q.c == a.nchunks) {
+      q.c = 0;
+      q.p += NW;
+      while (q.p >= a.nblk) {
+        q.p -= a.nblk;
+        ++q.u;
+      }
+    }
+  };
+  auto issue = [&](const ItemCur &q, int s) {
+    const int c = q.c, u = q.u, p = q.p;
     uint8_t *st = wring + s * a.stage_bytes;
     const uintptr_t slot_off = static_cast<uintptr_t>(pl.u_slot[u]) * static_cast<uintptr_t>(a.stride);
     uintptr_t src = 0;
@@ -531,8 +549,13 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const __grid_con
     warp_bulk_copies(dst, src, n, mend, &wbar[warp * kMaxNS + s], lane);
   };
 
-  int issued = 0;
-  for (; issued < a.NS - 1 && issued < n_items; ++issued) issue(issued, issued % a.NS);
+  int issued = 0, is = 0;
+  ItemCur ic = cur_first();
+  for (; issued < a.NS - 1 && issued < n_items; ++issued) {
+    issue(ic, is);
+    cur_next(ic);
+    is = (is + 1 == a.NS) ? 0 : is + 1;
+  }
 
   // activations of the tokens this CTA needs (the first weight stages are already in flight)
   bool x_ok = true;
@@ -577,15 +600,18 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const __grid_con
   bool ok = x_ok;
   float acc1[RR];
   f2 acc2[RR][TT];
-  int consumed = 0;
-  for (int item = 0; item < n_items; ++item) {
+  int consumed = 0, cs = 0, cph = 0;
+  ItemCur cc = cur_first();
+  int toff_u = -1;  // unit whose token offsets toff[] hold
+  uint32_t toff[TT];
+  for (int item = 0; item < n_items; ++item, cur_next(cc)) {
     if (issued < n_items) {
-      issue(issued, issued % a.NS);
+      issue(ic, is);
+      cur_next(ic);
+      is = (is + 1 == a.NS) ? 0 : is + 1;
       ++issued;
     }
-    const int i = item / a.nchunks, c = item - i * a.nchunks;
-    const long long rb = rbA + warp + static_cast<long long>(i) * NW;
-    const int u = static_cast<int>(rb / a.nblk), p = static_cast<int>(rb - static_cast<long long>(u) * a.nblk);
+    const int c = cc.c, u = cc.u, p = cc.p;
     const int ucnt = pl.u_cnt[u];
     if (c == 0) {
 #pragma unroll
@@ -595,8 +621,7 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const __grid_con
         for (int t = 0; t < TT; ++t) acc2[r][t] = mk2(0.f, 0.f);
       }
     }
-    const int cs = item % a.NS;
-    if (ok && !mbar_wait(&wbar[warp * kMaxNS + cs], (item / a.NS) & 1)) ok = false;
+    if (ok && !mbar_wait(&wbar[warp * kMaxNS + cs], static_cast<uint32_t>(cph))) ok = false;
     if (ok) {
       const int kel = min(a.K - c * a.KC, a.KC);
       const int gcount = (kel + D::SG - 1) / D::SG;
@@ -624,12 +649,14 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const __grid_con
           }
         }
       }
-      // shared-memory offsets of the unit's token rows
-      uint32_t toff[TT];
+      // shared-memory offsets of the unit's token rows (recomputed when the unit changes)
+      if (u != toff_u) {
+        toff_u = u;
 #pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        const int tslot = t >= ucnt ? 0 : DOWN ? (u - uA) * TT + t : pl.s_pairs[pl.u_first[u] + t] / a.k;
-        toff[t] = static_cast<uint32_t>(tslot * a.xrow_bytes);
+        for (int t = 0; t < TT; ++t) {
+          const int tslot = t >= ucnt ? 0 : DOWN ? (u - uA) * TT + t : pl.s_pairs[pl.u_first[u] + t] / a.k;
+          toff[t] = static_cast<uint32_t>(tslot * a.xrow_bytes);
+        }
       }
       const uint32_t xc0 = xs_s + static_cast<uint32_t>(c * gpc * (D::SG * 4));
       for (int g = 0; g < gcount; ++g) {
@@ -674,6 +701,10 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const __grid_con
     }
     __syncwarp();  // every lane is done with this slot before it is refilled
     ++consumed;
+    if (++cs == a.NS) {
+      cs = 0;
+      cph ^= 1;
+    }
 
     if (c == a.nchunks - 1) {
       // the unit's RR x TT row sums, reduce-scattered over the warp
@@ -977,13 +1008,15 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
   // consume(item, stage address) computes it.  After an expired wait the warp issues nothing
   // more and waits for what it has in flight before it exits.
   int issued = 0, waited = 0, ph_base = 0, ph_n = 0;
+  int islot = 0, wslot = 0, wph = 0;  // ring slot of the next issue / wait, and the wait's phase bit
   auto issue_next = [&](auto &&describe, int row_stride) {
     uintptr_t src = 0, mend = 0;
     uint32_t n = 0;
     if (lane < 8) describe(issued - ph_base, lane, src, n, mend);
-    uint8_t *dst = wring + (issued % a.NS) * a.stage_bytes + lane * row_stride;
-    warp_bulk_copies(dst, src, n, mend, &wbar[warp * kMaxNS + issued % a.NS], lane);
+    uint8_t *dst = wring + islot * a.stage_bytes + lane * row_stride;
+    warp_bulk_copies(dst, src, n, mend, &wbar[warp * kMaxNS + islot], lane);
     ++issued;
+    if (++islot == a.NS) islot = 0;
   };
   // begin issues up to `ahead` stages: NS - 1 (the next one is issued before each wait, into
   // the slot consumed last) or NS (a full ring; each slot is refilled right after it is
@@ -997,16 +1030,20 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
   };
   auto finish = [&](auto &&describe, int row_stride, auto &&consume) {
     const bool full = ph_ahead == a.NS;
+    // positions are waited for in order across the phases: waited == ph_base + it here
     for (int it = 0; it < ph_n && ok; ++it) {
       if (!full && issued - ph_base < ph_n) issue_next(describe, row_stride);
-      const int pos = ph_base + it;
-      if (!mbar_wait(&wbar[warp * kMaxNS + pos % a.NS], (pos / a.NS) & 1)) {
+      if (!mbar_wait(&wbar[warp * kMaxNS + wslot], static_cast<uint32_t>(wph))) {
         ok = false;
         break;
       }
-      consume(it, wring_s + static_cast<uint32_t>((pos % a.NS) * a.stage_bytes));
+      consume(it, wring_s + static_cast<uint32_t>(wslot * a.stage_bytes));
       __syncwarp();  // every lane is done with the slot before it is refilled
       ++waited;
+      if (++wslot == a.NS) {
+        wslot = 0;
+        wph ^= 1;
+      }
       if (full && issued - ph_base < ph_n) issue_next(describe, row_stride);
     }
   };
@@ -1015,13 +1052,14 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
   // gate row, row 1 the up row
   {
     const long long nb = static_cast<long long>(kv) * F;
-    const long long bA = static_cast<long long>(blockIdx.x) * nb / G, bB = static_cast<long long>(blockIdx.x + 1) * nb / G;
-    const int nrb = static_cast<int>(bB - bA);
+    const int bA = static_cast<int>(static_cast<long long>(blockIdx.x) * nb / G);
+    const int bB = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * nb / G);
+    const int nrb = bB - bA;
     const int n_items = warp < nrb ? (nrb - warp + NW - 1) / NW : 0;
-    auto pair_of = [&](int item, int &jv, int &i) {
-      const long long b = bA + warp + static_cast<long long>(item) * NW;
-      jv = static_cast<int>(b / F);
-      i = static_cast<int>(b - static_cast<long long>(jv) * F);
+    auto pair_of = [&](int item, int &jv, int &i) {  // kv * F < 2^31 (kv <= 32 picks)
+      const int b = bA + warp + item * NW;
+      jv = b / F;
+      i = b - jv * F;
     };
     auto row_src = [&](int jv, int i, int r) {
       return reinterpret_cast<uintptr_t>(r == 0 ? a.wg : a.wu) +
@@ -1326,6 +1364,7 @@ qg_status one_token_layer(int type, const float *xn, const float *wr, const void
   int qk = 0, bb = 0;
   qg_block_shape(type, &qk, &bb);
   if (!qg::aligned16(xn) || !qg::aligned16(wr) || !qg::aligned16(act) || !qg::aligned16(ws)) return QG_EUNSUPPORTED;
+  if (static_cast<long long>(k) * F > INT32_MAX) return QG_EUNSUPPORTED;  // row pairs are numbered in 32 bits
   OneArgs a{};
   a.xn = xn;
   a.wr = wr;
