@@ -468,8 +468,9 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const __grid_con
   // (or clear) their residual (down)
   if (blockIdx.x == 0) {
     if constexpr (!DOWN) {
-      for (int i = threadIdx.x; i < P * a.F; i += NW * 32)
-        if (pl.s_id[i / a.F] < 0) a.out[i] = 0.f;
+      for (int q = 0; q < P; ++q)
+        if (pl.s_id[q] < 0)
+          for (int i = threadIdx.x; i < a.F; i += NW * 32) a.out[static_cast<size_t>(q) * a.F + i] = 0.f;
     }
   }
 
@@ -953,8 +954,9 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
   const int kv = static_cast<int>(s_misc[1]);
   // a pick with a bad id has a zero act row
   if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < k * F; i += NW * 32)
-      if (s_slot[i / F] < 0) a.act[i] = 0.f;
+    for (int j = 0; j < k; ++j)
+      if (s_slot[j] < 0)
+        for (int i = threadIdx.x; i < F; i += NW * 32) a.act[static_cast<size_t>(j) * F + i] = 0.f;
 
   // hidden rows of phase 2 for this CTA, and their down rows into L2 now
   const int hA = static_cast<int>(static_cast<long long>(blockIdx.x) * H / G);
