@@ -907,28 +907,38 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
   float *s_l = part;  // the logits (part is free until phase 2)
   for (int e = threadIdx.x; e < a.E; e += NW * 32) s_l[e] = __ldcg(a.logits + e);
   __syncthreads();
-  for (int e = threadIdx.x; e < a.E; e += NW * 32) {
-    const float le = s_l[e];
-    int rank = 0;
-    for (int f = 0; f < a.E; ++f) {
-      const float lf = s_l[f];
-      rank += (lf > le || (lf == le && f < e)) ? 1 : 0;
+  {
+    // rank(e) in four partial counts over quarters of the experts, so that every warp of the
+    // CTA takes a share (the ring is idle until the gate/up stages: it holds the counts)
+    int *s_rk = reinterpret_cast<int *>(ring);  // [4][E]
+    const int QF = (a.E + 3) >> 2;
+    for (int idx = threadIdx.x; idx < 4 * a.E; idx += NW * 32) {
+      const int q = idx / a.E, e = idx - q * a.E;
+      const float le = s_l[e];
+      const int f1 = min(a.E, (q + 1) * QF);
+      int r = 0;
+      for (int f = q * QF; f < f1; ++f) {
+        const float lf = s_l[f];
+        r += (lf > le || (lf == le && f < e)) ? 1 : 0;
+      }
+      s_rk[idx] = r;
     }
-    if (rank < k) s_ids[rank] = e;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const float lmax = s_l[s_ids[0]];
-    float den = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const float ex = expf(s_l[s_ids[j]] - lmax);
-      den += ex;
-      s_w[j] = ex;
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += NW * 32) {
+      const int rank = s_rk[e] + s_rk[a.E + e] + s_rk[2 * a.E + e] + s_rk[3 * a.E + e];
+      if (rank < k) s_ids[rank] = e;
     }
-    for (int j = 0; j < k; ++j) s_w[j] = s_w[j] / den;
   }
   __syncthreads();
   if (warp == 0) {
+    // softmax over the picks: one exponential per lane, the denominator summed in pick order
+    // (the router's order, so the weights are the standalone router's bit for bit)
+    const float lmax = s_l[s_ids[0]];
+    const float ex = lane < k ? expf(s_l[s_ids[lane]] - lmax) : 0.f;
+    float den = 0.f;
+    for (int j = 0; j < k; ++j) den += __shfl_sync(0xFFFFFFFFu, ex, j);
+    const float wt = ex / den;
+    if (lane < k) s_w[lane] = wt;
     bool valid = false;
     int slot = -1;
     if (lane < k) {
@@ -941,7 +951,7 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
       s_slot[lane] = valid ? slot : -1;
       if (blockIdx.x == 0) {
         a.ids_out[lane] = s_ids[lane];
-        a.wts_out[lane] = s_w[lane];
+        a.wts_out[lane] = wt;
         if (!valid) moe_status(QG_STATUS_BIT_ID);
       }
     }
@@ -1332,6 +1342,7 @@ qg_status launch_one_token(OneArgs a, cudaStream_t s) {
   const long long ring = dev.smem_optin - 1024 - hdr - xbytes - part;
   const int NS = ring > 0 ? static_cast<int>(std::min<long long>(kMaxNS, ring / (NW * stage))) : 0;
   if (NS < 2) return QG_EUNSUPPORTED;
+  if (static_cast<long long>(NW) * NS * stage < 16LL * a.E) return QG_EUNSUPPORTED;  // the ranking's counts
   a.NS = NS;
   a.stage_bytes = static_cast<int>(stage);
   a.off_x = hdr;
