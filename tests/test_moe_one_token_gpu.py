@@ -126,3 +126,20 @@ def test_one_token_many_calls_one_workspace(qg):
         torch.cuda.synchronize()
         assert np.array_equal(x.cpu().numpy(), first)
     assert qg.device_status() == 0
+
+
+@pytest.mark.parametrize("E,k", [(5, 4), (13, 8), (40, 8), (97, 1)])
+def test_one_token_expert_counts_not_multiple_of_four(qg, oracle_lib, E, k):
+    """The fused ranking splits the experts into four quarters (the last one short or empty when
+    E is not a multiple of four): picks and weights still equal the standalone router's."""
+    H, F = 512, 96
+    ex = Experts(gs.Q8_0, E, H, F, seed=80 + E)
+    wr = gs.router_weights(E, H, seed=E)
+    xn = gs.activations(1, H, seed=E, stream=56)
+    x = gs.activations(1, H, seed=E, stream=57)
+    ids, wts, act, out = _layer(qg, ex, xn, wr, x, k)
+    assert qg.device_status() == 0
+    i2, w2, lg = _route(qg, xn, wr, k)
+    assert np.array_equal(i2, ids) and np.array_equal(w2, wts)
+    check_route(oracle_lib, xn, wr, k, ids, wts, lg, what=f"one token E={E} k={k}")
+    check_combine(oracle_lib, ex, ids, wts, act, x, k, out, what=f"one token E={E} k={k}")
