@@ -19,7 +19,7 @@
  *  - qwen35_moe_ssd.js (diskformer 0.5.4 -> 0.6.6), BATCH_KERNELS: token-major batches,
  *    y[t*M + m] = sum_k x[t*N + k] * W[m][k] (matmulQ8T).
  *
- * Readings where the pages leave a step open (each listed in the design notes):
+ * Readings where the pages leave a step open:
  *  - raw byte order of Q8_0 / Q4_0 blocks: f16 d first, then the codes (ggml block_q8_0 /
  *    block_q4_0); the pages only show the split planes.
  *  - Q4_K element value: the exact real d*sc*q - dmin*m rounded once to f32 (RNE).  Both
