@@ -357,6 +357,18 @@ def run_section(args):
     return 0
 
 
+def max_over_ranks(torch, dist, el, device):
+    """The job's time: every rank contributes its own elapsed seconds and gets the slowest."""
+    t = torch.tensor([el], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbps(bytes_per_rank_step, world, steps, el):
+    """Whole-job throughput: the bytes every rank streamed over the slowest rank's time."""
+    return bytes_per_rank_step * world * steps / el / 1e9
+
+
 def run_ours(args):
     import torch
 
@@ -412,10 +424,8 @@ def run_ours(args):
         el, clocks = timed()  # measured once more, as the timing rules ask
         clocks["remeasured"] = True
     if world > 1:
-        t = torch.tensor([el], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el = float(t.item())
-    value = wbytes * world * args.steps / el / 1e9
+        el = max_over_ranks(torch, dist, el, dev)
+    value = job_gbps(wbytes, world, args.steps, el)
     achieved = (wbytes + abytes) / (el / args.steps) / 1e9  # every launch in the step is this kernel
 
     # end to end: pinned host activations in, head logits out, every step
