@@ -399,7 +399,7 @@ def run_ours(args):
     abytes = step_act_bytes(args.layers, T)
     launches = 4 * args.layers + 1
 
-    qg.set_static_weights(args.weights == "static")
+    qg.set_static_weights(args.weights == "static", stream)
     g = capture(torch, lambda: D.step(T), stream)
     if qg.device_status() != 0:
         raise RuntimeError("device status set after the first step")
@@ -501,9 +501,9 @@ def run_detail(torch, qg, D, stream, args, hbm):
     out = {}
     wbytes = step_weight_bytes(args.layers)
     other = "ordered" if args.weights == "static" else "static"
-    prev = qg.set_static_weights(other == "static")
+    prev = qg.set_static_weights(other == "static", stream)
     g = capture(torch, lambda: D.step(args.tokens), stream)
-    qg.set_static_weights(prev)
+    qg.set_static_weights(prev, stream)
     steps = max(20, args.steps // 4)
     el = time_graph(torch, g, stream, steps, 3)
     gbs = wbytes * steps / el / 1e9

@@ -49,7 +49,7 @@ def load():
             "qg_strerror": ([I], ctypes.c_char_p),
             "qg_block_shape": ([I, P, P], I),
             "qg_device_status": ([P, I], I),
-            "qg_set_static_weights": ([I], I),
+            "qg_set_static_weights": ([S, I], I),
             "qgemv_q8_0": ([P, P, P, I64, I64, S], I),
             "qgemv_q4_0": ([P, P, P, I64, I64, S], I),
             "qgemv_q4_k": ([P, P, P, I64, I64, S], I),
@@ -111,10 +111,14 @@ def device_status(clear: bool = True) -> int:
     return v.value
 
 
-def set_static_weights(enable: bool) -> bool:
-    """Declare the weight buffers immutable: GEMVs may start streaming them before the
-    preceding kernel in the stream finishes.  Returns the previous setting."""
-    return bool(load().qg_set_static_weights(int(bool(enable))))
+def set_static_weights(enable: bool, stream=None) -> bool:
+    """Declare the weight buffers read on `stream` (default: the current stream) immutable:
+    GEMVs enqueued there may start streaming them before the preceding kernel finishes.
+    Returns the stream's previous setting."""
+    prev = load().qg_set_static_weights(_stream(stream), int(bool(enable)))
+    if prev < 0:
+        raise QGError(QG_ECUDA, "qg_set_static_weights")
+    return bool(prev)
 
 
 def row_bytes(qtype: int, n: int) -> int:

@@ -1,6 +1,5 @@
 // qg_abi.cu -- library-wide entry points: version, status strings, block shapes, device
 // status word, and the per-device property cache.
-#include <atomic>
 #include <mutex>
 
 #include "qg_host.h"
@@ -37,10 +36,30 @@ const DeviceInfo &device_info() {
 }
 
 namespace {
-std::atomic<int> g_static_weights{0};
-}
+// Streams whose callers declared their weights immutable (qg_set_static_weights), per device.
+// A small table searched per launch: a process holds a handful of streams.
+constexpr int kMaxStaticStreams = 256;
+struct StaticEntry {
+  cudaStream_t s;
+  int device;
+};
+std::mutex g_static_mu;
+StaticEntry g_static[kMaxStaticStreams];
+int g_static_n = 0;
 
-bool static_weights() { return g_static_weights.load(std::memory_order_relaxed) != 0; }
+int find_static(cudaStream_t s, int dev) {
+  for (int i = 0; i < g_static_n; ++i)
+    if (g_static[i].s == s && g_static[i].device == dev) return i;
+  return -1;
+}
+}  // namespace
+
+bool static_weights(cudaStream_t s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  return find_static(s, dev) >= 0;
+}
 
 bool set_smem_attr(const void *func, uint32_t bytes) {
   int dev = 0;
@@ -68,7 +87,7 @@ bool set_smem_attr(const void *func, uint32_t bytes) {
 
 extern "C" {
 
-int qg_version(void) { return 1; }
+int qg_version(void) { return 2; }
 
 const char *qg_strerror(int status) {
   switch (status) {
@@ -99,8 +118,20 @@ qg_status qg_block_shape(int type, int *qk, int *block_bytes) {
   return QG_OK;
 }
 
-int qg_set_static_weights(int enable) {
-  return qg::g_static_weights.exchange(enable ? 1 : 0) != 0;
+int qg_set_static_weights(qg_stream_t stream, int enable) {
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;  // no device: the handle alone is the key
+  std::lock_guard<std::mutex> lk(qg::g_static_mu);
+  const int i = qg::find_static(s, dev);
+  const int prev = i >= 0 ? 1 : 0;
+  if (enable && i < 0) {
+    if (qg::g_static_n >= qg::kMaxStaticStreams) return -1;
+    qg::g_static[qg::g_static_n++] = qg::StaticEntry{s, dev};
+  } else if (!enable && i >= 0) {
+    qg::g_static[i] = qg::g_static[--qg::g_static_n];
+  }
+  return prev;
 }
 
 qg_status qg_device_status(uint32_t *status_out, int clear) {

@@ -181,13 +181,41 @@ QG_DEVICE float magic_byte(uint32_t word, uint32_t byte_idx) {
   return __uint_as_float(__byte_perm(word, 0x4B000000u, 0x7440u | byte_idx));
 }
 
-// Packed f32x2 arithmetic (sm_100+): two IEEE f32 operations per instruction, through the
-// toolkit's float2 intrinsics so that operands live in register pairs.
+// Packed f32x2 arithmetic (sm_100+): two IEEE f32 operations per instruction, operands in
+// register pairs.  The flush-to-zero forms are used: a denormal f32 operand (|v| < 2^-126)
+// counts as zero.  The packed unit takes a slow path on denormal operands without it (about
+// 40x slower in a micro-benchmark), so activations with many denormals would slow every
+// product down.  Every weight the decoders produce is 0 or at least 2^-24 in magnitude (f16
+// scales times small integers), so only products with a denormal activation and denormal
+// partial sums are affected: each error is below 2^-126 * 2^23 (the largest decoded weight is
+// about 65504 * 127), far inside the 1e-6 absolute term of the output bound.
 using f2 = float2;
 QG_DEVICE f2 mk2(float a, float b) { return make_float2(a, b); }
-QG_DEVICE f2 add2(f2 a, f2 b) { return __fadd2_rn(a, b); }
-QG_DEVICE f2 mul2(f2 a, f2 b) { return __fmul2_rn(a, b); }
-QG_DEVICE f2 fma2(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
+QG_DEVICE unsigned long long pack2(f2 v) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+QG_DEVICE f2 unpack2(unsigned long long r) {
+  f2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+QG_DEVICE f2 add2(f2 a, f2 b) {
+  unsigned long long d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
+  return unpack2(d);
+}
+QG_DEVICE f2 mul2(f2 a, f2 b) {
+  unsigned long long d;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
+  return unpack2(d);
+}
+QG_DEVICE f2 fma2(f2 a, f2 b, f2 c) {
+  unsigned long long d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)), "l"(pack2(c)));
+  return unpack2(d);
+}
 
 // f16 bits -> f32 (exact; hardware conversion).
 QG_DEVICE float h2f(uint32_t bits16) {

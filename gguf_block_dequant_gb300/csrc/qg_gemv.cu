@@ -530,7 +530,7 @@ qg_status launch_cfg(int nmat, const void *const *w, const float *x, float *cons
   auto kern = qgemv_kernel<QT, TT, NW>;
   if (!qg::set_smem_attr(reinterpret_cast<const void *>(kern), smem)) return QG_ECUDA;
   const int grid = static_cast<int>(grid_ctas);
-  a.early_weights = qg::static_weights() ? 1 : 0;
+  a.early_weights = qg::static_weights(stream) ? 1 : 0;
   if (qg::launch_pdl(kern, dim3(grid), dim3(NW * 32), smem, stream, map, a) != cudaSuccess) return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }

@@ -44,8 +44,9 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// whether the caller declared its weights immutable (qg_set_static_weights)
-bool static_weights();
+// whether the caller declared the weights read by launches on stream s (on the current
+// device) immutable (qg_set_static_weights)
+bool static_weights(cudaStream_t s);
 
 // dense GEMV entry shared by qgemv_* / qgemv_t / qgemm (small T) / MoE helpers
 qg_status gemv_dispatch(int type, const void *w, const float *x, float *y, int64_t M, int64_t N, int T,

@@ -195,6 +195,7 @@ struct MoeArgs {
   int32_t *ids_out;
   float *wts_out;
   uint32_t off_plan, off_x, off_ring;
+  int plan_only;  // host side: check that the shapes fit the kernel's shared-memory plan, launch nothing
 };
 
 // Pairs grouped by expert.  s_id[z]: expert of pair z, or -1 when its id or slot is out of
@@ -1163,20 +1164,28 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
 // Host side
 // ------------------------------------------------------------------------------------------
 
+// Workspace layout.  A fixed header comes first, at offsets that do not depend on the shape
+// of a call: the one-token layer's grid-barrier counter (a 64-bit word that only grows) and
+// the router's tickets (one word per 16-token tile, room for every tile count the router
+// accepts).  Both must read zero in a fresh workspace and keep their meaning from call to
+// call, so one workspace sized for the largest shape serves every smaller one.  The scratch
+// regions (logits, dn rows, the grouped rows of the T > 16 path) follow the header and are
+// rewritten by every call.
+constexpr int kMaxRouterTiles = 65535;  // grid.y limit of the router launch
+constexpr size_t kWsBar = 0;
+constexpr size_t kWsTickets = 256;
+constexpr size_t kWsHeader = (kWsTickets + static_cast<size_t>(kMaxRouterTiles) * 4 + 255) & ~static_cast<size_t>(255);
+
 struct WsLayout {
-  size_t logits, ticket, bar, dn, tc, total;
+  size_t logits, dn, tc, total;
 };
 
 inline size_t up256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 WsLayout ws_layout(int T, int k, int E, int H, int F = 0) {
   WsLayout w;
-  w.logits = 0;
-  w.ticket = up256(static_cast<size_t>(T) * E * 4);
-  // router tickets, then the two words of the one-token layer's grid barrier
-  const size_t tickets = static_cast<size_t>((T + kRouterTB - 1) / kRouterTB) * 4;
-  w.bar = w.ticket + ((tickets + 15) & ~static_cast<size_t>(15));
-  w.dn = w.ticket + up256(((tickets + 15) & ~static_cast<size_t>(15)) + 16);
+  w.logits = kWsHeader;
+  w.dn = w.logits + up256(static_cast<size_t>(T) * E * 4);
   w.tc = w.dn + up256(static_cast<size_t>(T) * k * H * 4);
   w.total = w.tc;
   // grouped tensor-core path (more than 16 tokens): plan, grouped bf16 rows
@@ -1192,22 +1201,47 @@ qg_status check_common(int T, int k, int E, int H, int F) {
   return QG_OK;
 }
 
-qg_status route_impl(const float *xn, const float *wr, int T, int H, int E, int k, int32_t *ids, float *weights,
-                     float *logits_out, void *ws, size_t ws_bytes, cudaStream_t s, int do_topk = 1) {
-  if (!xn || !wr || !ids || !weights || !ws) return QG_EINVAL_PTR;
+// Argument checks of the router (everything but the workspace), run before anything is
+// enqueued.
+qg_status route_check(const float *xn, const float *wr, int T, int H, int E, int k, const int32_t *ids,
+                      const float *weights) {
+  if (!xn || !wr || !ids || !weights) return QG_EINVAL_PTR;
   if (T < 1 || k < 1 || k > kMaxK || E < k || E > kMaxE || H < 4 || H % 4) return QG_EINVAL_SHAPE;
   if (static_cast<long long>(T) * H > INT32_MAX || static_cast<long long>(T) * E > INT32_MAX) return QG_EINVAL_SHAPE;
-  if (!qg::aligned16(xn) || !qg::aligned16(wr) || !qg::aligned16(ws)) return QG_EALIGN;
-  const WsLayout L = ws_layout(T, 1, E, H);
-  if (ws_bytes < L.dn) return QG_EWORKSPACE;
-  uint8_t *w = static_cast<uint8_t *>(ws);
-  float *logits = logits_out ? logits_out : reinterpret_cast<float *>(w + L.logits);
+  if ((T + kRouterTB - 1) / kRouterTB > kMaxRouterTiles) return QG_EINVAL_SHAPE;
+  if (!qg::aligned16(xn) || !qg::aligned16(wr)) return QG_EALIGN;
+  return QG_OK;
+}
+
+// Router launch (route_check passed): logits into `logits` ([T][E]); with do_topk the last
+// CTA of each token tile takes the picks, counting arrivals on tickets[tile] (zero on entry,
+// zero again on exit).
+qg_status route_launch(const float *xn, const float *wr, int T, int H, int E, int k, int32_t *ids, float *weights,
+                       float *logits, unsigned int *tickets, int do_topk, cudaStream_t s) {
   const dim3 grid(E, (T + kRouterTB - 1) / kRouterTB);
-  if (grid.y > 65535) return QG_EINVAL_SHAPE;
   if (qg::launch_pdl(moe_router_kernel, grid, dim3(kRouterWarps * 32), 0, s, xn, wr, T, H, E, k, logits, ids, weights,
-                     reinterpret_cast<unsigned int *>(w + L.ticket), do_topk) != cudaSuccess)
+                     tickets, do_topk) != cudaSuccess)
     return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+}
+
+qg_status ws_check(const void *ws, size_t ws_bytes, size_t need) {
+  if (!ws) return QG_EWORKSPACE;
+  if (!qg::aligned16(ws)) return QG_EALIGN;
+  return ws_bytes < need ? QG_EWORKSPACE : QG_OK;
+}
+
+qg_status route_impl(const float *xn, const float *wr, int T, int H, int E, int k, int32_t *ids, float *weights,
+                     float *logits_out, void *ws, size_t ws_bytes, cudaStream_t s, int do_topk = 1) {
+  qg_status c = route_check(xn, wr, T, H, E, k, ids, weights);
+  if (c != QG_OK) return c;
+  const WsLayout L = ws_layout(T, 1, E, H);
+  c = ws_check(ws, ws_bytes, L.dn);
+  if (c != QG_OK) return c;
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  float *logits = logits_out ? logits_out : reinterpret_cast<float *>(w + L.logits);
+  return route_launch(xn, wr, T, H, E, k, ids, weights, logits, reinterpret_cast<unsigned int *>(w + kWsTickets),
+                      do_topk, s);
 }
 
 template <int QT, int TT, bool DOWN>
@@ -1269,6 +1303,7 @@ qg_status launch_expert(MoeArgs a, cudaStream_t s) {
   }
   a.NS = static_cast<int>(std::min<long long>(kMaxNS, ring_avail / (static_cast<long long>(NW) * a.stage_bytes)));
   if (a.NS < 2) return QG_EUNSUPPORTED;
+  if (a.plan_only) return QG_OK;
   a.off_ring = static_cast<uint32_t>(a.off_x + xbytes);
   const uint32_t smem = a.off_ring + static_cast<uint32_t>(NW * a.NS * a.stage_bytes) + 1024 + 64;
   // one token: tensor map over the activation rows ([rows * K / 32][32] f32, 128-byte swizzle)
@@ -1354,7 +1389,7 @@ qg_status launch_one_token(OneArgs a, cudaStream_t s) {
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem) != cudaSuccess || per_sm < 1)
     return QG_EUNSUPPORTED;
-  a.early_weights = qg::static_weights() ? 1 : 0;
+  a.early_weights = qg::static_weights(s) ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(G);
   cfg.blockDim = dim3(NW * 32);
@@ -1401,7 +1436,7 @@ qg_status one_token_layer(int type, const float *xn, const float *wr, const void
   a.x = x_inout;
   const WsLayout L = ws_layout(1, k, E, H, F);
   a.logits = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + L.logits);
-  a.bar = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(ws) + L.bar);
+  a.bar = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(ws) + kWsBar);
   a.rbh = static_cast<long long>(H / qk) * bb;
   a.rbf = static_cast<long long>(F / qk) * bb;
   switch (type) {
@@ -1425,10 +1460,11 @@ qg_status expert_checks(int type, int T, int k, int E, int H, int F, int n_slots
   return QG_OK;
 }
 
-qg_status swiglu_impl(int type, const void *w_gate, const void *w_up, int64_t stride, const int32_t *slots,
-                      int n_slots, int E, const int32_t *ids, const float *xn, int T, int k, int H, int F,
-                      float *act, void *ws, size_t ws_bytes, cudaStream_t s, const float *fused_logits = nullptr,
-                      int32_t *ids_out = nullptr, float *wts_out = nullptr) {
+// Host checks of the gate/up step that need no launch; the shared-memory plan is checked by
+// swiglu_plan.  Nothing is enqueued by either.
+qg_status swiglu_check(int type, const void *w_gate, const void *w_up, int64_t stride, int n_slots, int E,
+                       const int32_t *ids, const float *xn, int T, int k, int H, int F, const float *act,
+                       const void *ws, size_t ws_bytes) {
   if (!w_gate || !w_up || !ids || !xn || !act) return QG_EINVAL_PTR;
   const qg_status c = expert_checks(type, T, k, E, H, F, n_slots, stride);
   if (c != QG_OK) return c;
@@ -1438,13 +1474,17 @@ qg_status swiglu_impl(int type, const void *w_gate, const void *w_up, int64_t st
   const long long mat = static_cast<long long>(F) * (H / qk) * bb;
   if (n_slots > 1 && stride < mat) return QG_EINVAL_SHAPE;
   if (T > 16) {
-    if (!ws) return QG_EINVAL_PTR;
-    if (!qg::aligned16(ws) || !qg::aligned16(w_gate) || !qg::aligned16(w_up)) return QG_EALIGN;
-    const WsLayout L = ws_layout(T, k, E, H, F);
-    if (ws_bytes < L.total) return QG_EWORKSPACE;
-    return qg::moe_swiglu_tc(w_gate, w_up, stride, slots, n_slots, E, ids, xn, T, k, H, F, act,
-                             static_cast<uint8_t *>(ws) + L.tc, s);
+    if (!qg::aligned16(w_gate) || !qg::aligned16(w_up)) return QG_EALIGN;
+    return ws_check(ws, ws_bytes, ws_layout(T, k, E, H, F).total);
   }
+  return QG_OK;
+}
+
+MoeArgs swiglu_args(int type, const void *w_gate, const void *w_up, int64_t stride, const int32_t *slots,
+                    int n_slots, int E, const int32_t *ids, const float *xn, int T, int k, int H, int F, float *act) {
+  int qk = 0, bb = 0;
+  qg_block_shape(type, &qk, &bb);
+  const long long mat = static_cast<long long>(F) * (H / qk) * bb;
   MoeArgs a{};
   a.wa = static_cast<const uint8_t *>(w_gate);
   a.wb = static_cast<const uint8_t *>(w_up);
@@ -1463,6 +1503,22 @@ qg_status swiglu_impl(int type, const void *w_gate, const void *w_up, int64_t st
   a.F = F;
   a.K = H;
   a.R = F;
+  return a;
+}
+
+qg_status swiglu_impl(int type, const void *w_gate, const void *w_up, int64_t stride, const int32_t *slots,
+                      int n_slots, int E, const int32_t *ids, const float *xn, int T, int k, int H, int F,
+                      float *act, void *ws, size_t ws_bytes, cudaStream_t s, const float *fused_logits = nullptr,
+                      int32_t *ids_out = nullptr, float *wts_out = nullptr, int plan_only = 0) {
+  const qg_status c = swiglu_check(type, w_gate, w_up, stride, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes);
+  if (c != QG_OK) return c;
+  if (T > 16) {
+    if (plan_only) return QG_OK;
+    return qg::moe_swiglu_tc(w_gate, w_up, stride, slots, n_slots, E, ids, xn, T, k, H, F, act,
+                             static_cast<uint8_t *>(ws) + ws_layout(T, k, E, H, F).tc, s);
+  }
+  MoeArgs a = swiglu_args(type, w_gate, w_up, stride, slots, n_slots, E, ids, xn, T, k, H, F, act);
+  a.plan_only = plan_only;
   if (fused_logits) {
     a.fuse_topk = 1;
     a.logits = fused_logits;
@@ -1472,25 +1528,38 @@ qg_status swiglu_impl(int type, const void *w_gate, const void *w_up, int64_t st
   return launch_expert_type<false>(type, a, s);
 }
 
-qg_status combine_impl(int type, const void *w_down, int64_t stride, const int32_t *slots, int n_slots, int E,
-                       const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
-                       float *x_inout, int add_residual, void *ws, size_t ws_bytes, cudaStream_t s) {
-  if (!w_down || !ids || !weights || !act || !x_inout || !ws) return QG_EINVAL_PTR;
+qg_status combine_check(int type, const void *w_down, int64_t stride, int n_slots, int E, const int32_t *ids,
+                        const float *weights, const float *act, int T, int k, int H, int F, const float *x_inout,
+                        const void *ws, size_t ws_bytes) {
+  if (!w_down || !ids || !weights || !act || !x_inout) return QG_EINVAL_PTR;
   const qg_status c = expert_checks(type, T, k, E, H, F, n_slots, stride);
   if (c != QG_OK) return c;
-  if (!qg::aligned16(act) || !qg::aligned16(ws)) return QG_EALIGN;
-  const WsLayout L = ws_layout(T, k, E, H, F);
-  if (ws_bytes < L.total) return QG_EWORKSPACE;
+  if (!qg::aligned16(act) || !qg::aligned16(x_inout)) return QG_EALIGN;
+  if (T > 16 && !qg::aligned16(w_down)) return QG_EALIGN;
   int qk = 0, bb = 0;
   qg_block_shape(type, &qk, &bb);
   const long long mat = static_cast<long long>(H) * (F / qk) * bb;
   if (n_slots > 1 && stride < mat) return QG_EINVAL_SHAPE;
+  return ws_check(ws, ws_bytes, ws_layout(T, k, E, H, F).total);
+}
+
+qg_status combine_impl(int type, const void *w_down, int64_t stride, const int32_t *slots, int n_slots, int E,
+                       const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
+                       float *x_inout, int add_residual, void *ws, size_t ws_bytes, cudaStream_t s,
+                       int plan_only = 0) {
+  const qg_status c =
+      combine_check(type, w_down, stride, n_slots, E, ids, weights, act, T, k, H, F, x_inout, ws, ws_bytes);
+  if (c != QG_OK) return c;
+  const WsLayout L = ws_layout(T, k, E, H, F);
   uint8_t *w = static_cast<uint8_t *>(ws);
   if (T > 16) {
-    if (!qg::aligned16(x_inout) || !qg::aligned16(w_down)) return QG_EALIGN;
+    if (plan_only) return QG_OK;
     return qg::moe_combine_tc(w_down, stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout,
                               add_residual ? 1 : 0, reinterpret_cast<float *>(w + L.dn), w + L.tc, s);
   }
+  int qk = 0, bb = 0;
+  qg_block_shape(type, &qk, &bb);
+  const long long mat = static_cast<long long>(H) * (F / qk) * bb;
   MoeArgs a{};
   a.wa = static_cast<const uint8_t *>(w_down);
   a.wb = a.wa;
@@ -1512,9 +1581,9 @@ qg_status combine_impl(int type, const void *w_down, int64_t stride, const int32
   a.K = F;
   a.R = H;
   a.add_residual = add_residual ? 1 : 0;
+  a.plan_only = plan_only;
   const qg_status r = launch_expert_type<true>(type, a, s);
-  if (r != QG_OK) return r;
-  if (!qg::aligned16(x_inout) || H % 4) return QG_EALIGN;
+  if (r != QG_OK || plan_only) return r;
   return qg::moe_launch_combine(a.dn, weights, ids, slots, n_slots, E, T, k, H, x_inout, add_residual ? 1 : 0, s);
 }
 
@@ -1533,18 +1602,21 @@ unsigned int read_status_moe(bool clear) {
 }  // namespace qg
 
 // ---- router without a caller workspace -----------------------------------------------------
-// Fixed device scratch for moe_route_topk_noalloc: the router's logits and its per-tile
-// tickets, laid out exactly as the workspace of moe_route_topk.  Sized for T * E <= 16384
-// logits and 1024 token tiles (68 KB).
+// Fixed device scratch for moe_route_topk_noalloc: the per-tile tickets (1024 words) and then
+// the logits (16384 floats), 68 KB in all.  Every device that loads the library holds one copy
+// until the process exits.
 namespace {
 constexpr int kNoAllocLogits = 16384;
 constexpr int kNoAllocTiles = 1024;
-constexpr size_t kNoAllocBytes = static_cast<size_t>(kNoAllocLogits) * 4 + static_cast<size_t>(kNoAllocTiles) * 4;
+constexpr size_t kNoAllocTicketBytes = static_cast<size_t>(kNoAllocTiles) * 4;
+constexpr size_t kNoAllocBytes = kNoAllocTicketBytes + static_cast<size_t>(kNoAllocLogits) * 4;
 __device__ __align__(256) unsigned char g_route_scratch[kNoAllocBytes];
 
 std::mutex g_scratch_mu;
 void *g_scratch_ptr[64];  // per device, filled on the first call with that device current
 
+// Device address of the scratch array on the current device.  In host code the array's name
+// is only a stand-in, so the address comes from the runtime, once per device.
 void *route_scratch() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
@@ -1562,18 +1634,20 @@ extern "C" {
 
 qg_status moe_route_topk_noalloc(const float *xn, const float *wr, int T, int H, int E, int k, int32_t *ids,
                                  float *weights, float *logits_out, qg_stream_t stream) {
-  if (T < 1 || E < 1 || static_cast<long long>(T) * E > kNoAllocLogits ||
-      (T + kRouterTB - 1) / kRouterTB > kNoAllocTiles)
-    return QG_EWORKSPACE;
+  // every check before anything is enqueued
+  const qg_status c = route_check(xn, wr, T, H, E, k, ids, weights);
+  if (c != QG_OK) return c;
+  const int tiles = (T + kRouterTB - 1) / kRouterTB;
+  if (static_cast<long long>(T) * E > kNoAllocLogits || tiles > kNoAllocTiles) return QG_EWORKSPACE;
   void *ws = route_scratch();
   if (!ws) return QG_ECUDA;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const WsLayout L = ws_layout(T, 1, E, H);
-  // the tickets must read zero when the router starts: clear them for this shape's layout
-  if (cudaMemsetAsync(static_cast<uint8_t *>(ws) + L.ticket, 0,
-                      static_cast<size_t>((T + kRouterTB - 1) / kRouterTB) * 4, s) != cudaSuccess)
-    return QG_ECUDA;
-  return route_impl(xn, wr, T, H, E, k, ids, weights, logits_out, ws, kNoAllocBytes, s);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  // the tickets must read zero when the router starts (the previous call may have had another
+  // shape, or may not have finished its tiles)
+  if (cudaMemsetAsync(w, 0, static_cast<size_t>(tiles) * 4, s) != cudaSuccess) return QG_ECUDA;
+  float *logits = logits_out ? logits_out : reinterpret_cast<float *>(w + kNoAllocTicketBytes);
+  return route_launch(xn, wr, T, H, E, k, ids, weights, logits, reinterpret_cast<unsigned int *>(w), 1, s);
 }
 
 size_t moe_workspace_size(int T, int k, int E, int H, int F) {
@@ -1606,10 +1680,14 @@ qg_status moe_layer(int type, const float *xn, const float *wr, const void *w_ga
                     int E, int k, int32_t *ids, float *weights, float *act, float *x_inout, void *ws,
                     size_t ws_bytes, qg_stream_t stream) {
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (!xn || !wr || !w_gate || !w_up || !w_down || !ids || !weights || !act || !x_inout || !ws) return QG_EINVAL_PTR;
-  const qg_status c = expert_checks(type, T, k, E, H, F, n_slots, expert_stride);
+  // every step's checks (and, for T <= 16, its shared-memory plan) before the first launch
+  if (!xn || !wr || !w_gate || !w_up || !w_down || !ids || !weights || !act || !x_inout) return QG_EINVAL_PTR;
+  qg_status c = route_check(xn, wr, T, H, E, k, ids, weights);
   if (c != QG_OK) return c;
-  if (ws_bytes < ws_layout(T, k, E, H, F).total) return QG_EWORKSPACE;
+  c = swiglu_check(type, w_gate, w_up, expert_stride, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes);
+  if (c != QG_OK) return c;
+  c = combine_check(type, w_down, expert_stride, n_slots, E, ids, weights, act, T, k, H, F, x_inout, ws, ws_bytes);
+  if (c != QG_OK) return c;
   qg_status r;
   if (T > 16) {
     // prefill-sized batch: router with top-k, then the grouped tensor-core expert steps
@@ -1628,9 +1706,15 @@ qg_status moe_layer(int type, const float *xn, const float *wr, const void *w_ga
   }
   // router logits into the workspace; the gate/up kernel ranks them (every CTA needs the
   // picks for its plan anyway) and stores ids and weights for the combine
+  const float *logits = reinterpret_cast<const float *>(static_cast<uint8_t *>(ws) + ws_layout(T, k, E, H).logits);
+  r = swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes, s,
+                  logits, ids, weights, 1);
+  if (r != QG_OK) return r;
+  r = combine_impl(type, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout, 1, ws,
+                   ws_bytes, s, 1);
+  if (r != QG_OK) return r;
   r = route_impl(xn, wr, T, H, E, k, ids, weights, nullptr, ws, ws_bytes, s, 0);
   if (r != QG_OK) return r;
-  const float *logits = reinterpret_cast<const float *>(static_cast<uint8_t *>(ws) + ws_layout(T, k, E, H).logits);
   r = swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes, s,
                   logits, ids, weights);
   if (r != QG_OK) return r;

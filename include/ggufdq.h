@@ -92,18 +92,23 @@ QG_API qg_status qg_block_shape(int type, int *qk, int *block_bytes);
  * Synchronises the device.  When `clear` is non-zero the word is reset to 0. */
 QG_API qg_status qg_device_status(uint32_t *status_out, int clear);
 
-/* Static weights (process-wide switch, off by default).  Every launch of this library waits
- * for the preceding kernel in its stream (programmatic dependent launch) before it touches
- * memory.  A caller whose weight buffers are immutable model parameters - written once,
- * before any GEMV that reads them, and never by a kernel enqueued ahead of a GEMV in the
- * same stream - may call qg_set_static_weights(1): the dense GEMVs (qgemv_* and
- * qgemv_multi) then start streaming their first weight tiles into shared memory while the
- * preceding kernel drains, and only the activations and outputs wait for it.  Leave it off
- * when a kernel in the stream may write the weights (quantise-in-place, a loader that copies
- * through a kernel): the GEMV could read stale bytes.  Host-to-device copies are ordered
- * either way.  Takes effect for launches enqueued after the call; returns the previous
- * setting (0 or 1). */
-QG_API int qg_set_static_weights(int enable);
+/* Static weights, a setting of one stream (off by default).  Every launch of this library
+ * waits for the preceding kernel in its stream (programmatic dependent launch) before it
+ * touches memory.  A caller whose weight buffers are immutable model parameters - written
+ * once, before any GEMV that reads them, and never by a kernel enqueued ahead of a GEMV in
+ * the same stream - may call qg_set_static_weights(stream, 1): the dense GEMVs (qgemv_*,
+ * qgemv_t, qgemv_multi) and the one-token MoE layer enqueued on that stream then start
+ * streaming their first weight tiles while the preceding kernel drains, and only the
+ * activations and outputs wait for it.  Leave it off when a kernel in the stream may write
+ * the weights (quantise-in-place, a loader that copies through a kernel): the GEMV could read
+ * stale bytes.  Host-to-device copies are ordered either way.
+ *   - The setting belongs to the (device, stream handle) pair that is current at the call,
+ *     and other streams and other users of the library in the process are not affected.
+ *     Clear it before destroying the stream: a new stream may reuse the handle.
+ *   - It takes effect for launches enqueued (or captured) after the call.
+ *   - Returns the previous setting of that stream (0 or 1), or -1 when 256 streams already
+ *     hold the setting. */
+QG_API int qg_set_static_weights(qg_stream_t stream, int enable);
 
 /* ---- dense quantized GEMV, one token ----------------------------------------------------
  * y[m] = sum_k W[m][k] * x[k] for m < M  (matmulQ8 / matmulQ4 / matmulQ6K on the pages, and
@@ -155,9 +160,15 @@ QG_API qg_status qgemm(int type, const void *w, const float *x, float *y, int64_
  * Pairs z = t*k + j index the per-pick buffers (act is f32 [T*k][F]).
  *
  * Workspace: moe_workspace_size(T, k, E, H, F) bytes of device memory, 16-byte aligned,
- * zero-filled by the caller once before its first use (it holds the router's per-tile
- * tickets, which every call leaves at zero again); it also holds the router logits, the
- * per-pick down rows and, for more than 16 tokens, the grouped bf16 rows.  Calls that share a
+ * zero-filled by the caller once before its first use.  Its first 256.25 KB are a fixed
+ * header whose words keep their meaning from call to call: the one-token layer's grid-barrier
+ * counter (a 64-bit word that every moe_layer call at T = 1 advances) and the router's
+ * per-tile tickets (every call leaves them at zero again).  Their offsets do not depend on the
+ * call's shape, so one workspace sized for the largest shape it will serve (the largest T, k,
+ * E, H, F) may serve any call whose moe_workspace_size is not larger.  The rest holds scratch
+ * that each call rewrites: the router logits, the per-pick down rows and, for more than 16
+ * tokens, the grouped bf16 rows.  A NULL, misaligned or too small workspace returns
+ * QG_EWORKSPACE (QG_EALIGN when misaligned) with nothing launched.  Calls that share a
  * workspace must not run concurrently. */
 QG_API size_t moe_workspace_size(int T, int k, int E, int H, int F);
 
@@ -174,13 +185,15 @@ QG_API qg_status moe_route_topk(const float *xn, const float *wr, int T, int H, 
 /* The router of moe_route_topk for callers that cannot hand the library a workspace: for
  * instance a host engine whose device memory is entirely reserved by its own allocator before
  * it calls in, or a binding that exposes only input and output tensors.  The library keeps a
- * fixed 68 KB scratch area in device memory for the logits and the per-tile tickets and
+ * fixed 68 KB scratch area in device memory (1024 ticket words, then 16384 logits) and
  * allocates nothing (no cudaMalloc, no allocating library call).
- *   - Limits: T * E <= 16384 and at most 1024 tiles of 16 tokens; larger shapes return
- *     QG_EWORKSPACE.
+ *   - Limits: T * E <= 16384 and T <= 16384 (at most 1024 tiles of 16 tokens); larger shapes
+ *     return QG_EWORKSPACE.  Every other argument check is moe_route_topk's, and all of them
+ *     run before anything is enqueued.
  *   - The scratch address is looked up once per device, on the first call with that device
  *     current; make that first call before any stream capture.
- *   - Each call clears the tickets of its shape on `stream` before the router runs.
+ *   - Each call clears the tickets of its shape on `stream` (one memset) before the router
+ *     runs; with logits_out == NULL the logits live in the scratch area.
  *   - One scratch area per device: calls that overlap (other streams, other host threads)
  *     race on it and must be serialised by the caller.
  * Results are the same as moe_route_topk's.  The engine pages have no counterpart: their

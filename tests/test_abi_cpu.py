@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_strings_and_block_shapes(lib):
-    assert lib.qg_version() == 1
+    assert lib.qg_version() == 2
     lib.qg_strerror.restype = ctypes.c_char_p
     assert lib.qg_strerror(0) == b"ok"
     assert lib.qg_strerror(999) == b"unknown status"
@@ -72,9 +72,13 @@ def test_moe_host_checks_need_no_gpu(lib):
     lib.moe_route_topk.argtypes = [P, P, I, I, I, I, P, P, P, P, SZ, P]
     lib.moe_expert_swiglu.argtypes = [I, P, P, I64, P, I, I, P, P, I, I, I, I, P, P, SZ, P]
     lib.moe_combine.argtypes = [I, P, I64, P, I, I, P, P, P, I, I, I, I, P, I, P, SZ, P]
-    # workspace: router logits + tickets + dn rows, each rounded to 256 bytes
+    # workspace: the fixed header (grid-barrier word, then one ticket word for each of up to
+    # 65535 router tiles), then router logits and dn rows, each rounded up to 256 bytes
+    header = (256 + 65535 * 4 + 255) // 256 * 256
     n = lib.moe_workspace_size(8, 8, 128, 2048, 768)
-    assert n == 4096 + 256 + 8 * 8 * 2048 * 4
+    assert n == header + 8 * 128 * 4 + 8 * 8 * 2048 * 4
+    # a workspace sized for a larger shape covers every smaller one
+    assert lib.moe_workspace_size(1, 8, 128, 2048, 768) < n
     assert lib.moe_workspace_size(8, 33, 128, 2048, 768) == 0   # k > 32
     assert lib.moe_workspace_size(8, 8, 300, 2048, 768) == 0    # E > 256
     fake = P(4096)
@@ -92,14 +96,52 @@ def test_moe_host_checks_need_no_gpu(lib):
                            None) == 8  # workspace too small
 
 
-def test_static_weights_switch_returns_previous_setting(lib):
-    lib.qg_set_static_weights.argtypes = [ctypes.c_int]
+def test_moe_rejects_before_enqueueing_anything(lib):
+    """Every check runs before the first launch: on a machine without a GPU a launch attempt
+    would return QG_ECUDA, so the argument error itself coming back shows that nothing was
+    enqueued ahead of it."""
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.moe_combine.argtypes = [I, P, I64, P, I, I, P, P, P, I, I, I, I, P, I, P, SZ, P]
+    lib.moe_route_topk_noalloc.argtypes = [P, P, I, I, I, I, P, P, P, P]
+    lib.moe_layer.argtypes = [I, P, P, P, P, P, I64, P, I, I, I, I, I, I, P, P, P, P, P, SZ, P]
+    lib.moe_workspace_size.argtypes = [I, I, I, I, I]
+    lib.moe_workspace_size.restype = SZ
+    fake, odd = P(1 << 20), P((1 << 20) + 4)
+    T, k, E, H, F = 4, 2, 8, 64, 32
+    big = 1 << 30
+    # misaligned x_inout: the down kernel must not be enqueued first
+    assert lib.moe_combine(8, fake, 0, None, 1, E, fake, fake, fake, T, k, H, F, odd, 1, fake, big, None) == 3
+    # the whole layer, misaligned act or x_inout, for each token-count path
+    for t in (1, 4, 17):
+        h, f = (256, 256) if t > 16 else (H, F)
+        assert lib.moe_layer(8, fake, fake, fake, fake, fake, 0, None, 1, t, h, f, E, k, fake, fake, odd, fake,
+                             fake, big, None) == 3, t
+        assert lib.moe_layer(8, fake, fake, fake, fake, fake, 0, None, 1, t, h, f, E, k, fake, fake, fake, odd,
+                             fake, big, None) == 3, t
+        assert lib.moe_layer(8, fake, fake, fake, fake, fake, 0, None, 1, t, h, f, E, k, fake, fake, fake, fake,
+                             fake, 16, None) == 8, t  # workspace too small
+    # the router without a workspace: argument errors before its ticket memset
+    assert lib.moe_route_topk_noalloc(odd, fake, 1, 64, 8, 2, fake, fake, None, None) == 3
+    assert lib.moe_route_topk_noalloc(fake, fake, 1, 64, 8, 9, fake, fake, None, None) == 1  # k > E
+    assert lib.moe_route_topk_noalloc(None, fake, 1, 64, 8, 2, fake, fake, None, None) == 2
+    # its limits: T * E <= 16384 and at most 1024 tiles of 16 tokens
+    assert lib.moe_route_topk_noalloc(fake, fake, 16385, 64, 1, 1, fake, fake, None, None) == 8
+    assert lib.moe_route_topk_noalloc(fake, fake, 200, 64, 128, 8, fake, fake, None, None) == 8
+
+
+def test_static_weights_is_a_setting_of_one_stream(lib):
+    """Each stream handle keeps its own setting; enabling it on one stream leaves the others
+    (and the legacy default stream) off.  No CUDA work is enqueued, so fake handles serve."""
+    lib.qg_set_static_weights.argtypes = [ctypes.c_void_p, ctypes.c_int]
     lib.qg_set_static_weights.restype = ctypes.c_int
-    prev = lib.qg_set_static_weights(0)
+    a, b = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000)
     try:
-        assert lib.qg_set_static_weights(7) == 0  # any non-zero value enables it
-        assert lib.qg_set_static_weights(1) == 1
-        assert lib.qg_set_static_weights(0) == 1
-        assert lib.qg_set_static_weights(0) == 0
+        assert lib.qg_set_static_weights(a, 7) == 0  # any non-zero value enables it
+        assert lib.qg_set_static_weights(a, 1) == 1
+        assert lib.qg_set_static_weights(b, 0) == 0  # the other stream is untouched
+        assert lib.qg_set_static_weights(None, 0) == 0
+        assert lib.qg_set_static_weights(a, 0) == 1
+        assert lib.qg_set_static_weights(a, 0) == 0
     finally:
-        lib.qg_set_static_weights(prev)
+        lib.qg_set_static_weights(a, 0)
+        lib.qg_set_static_weights(b, 0)

@@ -7,6 +7,7 @@ every dequantized weight comes out of the kernels bit-exact.
 import numpy as np
 import pytest
 
+import edge_blocks as eb
 import gguf_synth as gs
 from helpers import assert_within_bound, to_dev
 
@@ -79,6 +80,38 @@ def test_gemv_one_hot_is_exact_dequant(qg, oracle_lib, qtype):
                 # equal as values: exact for every nonzero weight; a zero weight may come out
                 # as +0 where the decoded value is -0 (negative Q6_K scales)
                 assert np.array_equal(y[t], W[:, k]), (qtype, T, k)
+
+
+@pytest.mark.parametrize("qtype", TYPES)
+@pytest.mark.parametrize("T", [1, 8, 16])
+@pytest.mark.parametrize("aligned", [False, True])
+def test_gemv_one_hot_edge_blocks(qg, oracle_lib, qtype, T, aligned):
+    """The formats' edge values through every CUDA decoder: Q8_0 code 0x80 (-128), negative,
+    subnormal and extreme f16 d; Q4_0 negative (ggml's d = max / -8), subnormal and largest d;
+    Q4_K d = 0, dmin = 0, all-63 scales and mins, subnormal and negative d; Q6_K scales -32 and
+    31 with subnormal and extreme d.  The blocks (tests/golden/hand_blocks.txt and
+    tests/edge_blocks.py, pinned on the CPU) are dealt over the rows between random blocks;
+    with one-hot activations every output equals one dequantized weight, bit for bit."""
+    qk, bb = gs.BLOCK[qtype]
+    # rows whose byte length is a multiple of 16 take the lean one-token kernel; the others
+    # the general one
+    if qk == 32:
+        N = 1024 if aligned else 640
+    else:
+        N = 2048 if aligned or qtype == gs.Q4_K else 1280
+    assert ((N // qk) * bb % 16 == 0) == (aligned or qtype == gs.Q4_K)
+    M = 26
+    w = eb.matrix_with_edge_blocks(qtype, M, N, seed=9)
+    W = oracle_lib.dequant(qtype, w, M, N)
+    cols = list(range(0, N, 5)) + [N - 1]
+    for start in range(0, len(cols), T):
+        ks = cols[start:start + T]
+        x = np.zeros((len(ks), N), np.float32)
+        for t, k in enumerate(ks):
+            x[t, k] = 1.0
+        y = _run(qg, qtype, w, x, M, N)
+        for t, k in enumerate(ks):
+            assert np.array_equal(y[t], W[:, k]), (qtype, T, k, np.nonzero(y[t] != W[:, k])[0][:4])
 
 
 @pytest.mark.parametrize("qtype", TYPES)

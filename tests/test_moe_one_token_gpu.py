@@ -4,6 +4,7 @@ slot is invalid, and many calls on one workspace (its grid-barrier counter only 
 import numpy as np
 import pytest
 
+import edge_blocks as eb
 import gguf_synth as gs
 from helpers import to_dev
 from test_moe_gpu import Experts, _act_bound, _route, _ws, check_combine, check_route, check_swiglu
@@ -143,3 +144,76 @@ def test_one_token_expert_counts_not_multiple_of_four(qg, oracle_lib, E, k):
     assert np.array_equal(i2, ids) and np.array_equal(w2, wts)
     check_route(oracle_lib, xn, wr, k, ids, wts, lg, what=f"one token E={E} k={k}")
     check_combine(oracle_lib, ex, ids, wts, act, x, k, out, what=f"one token E={E} k={k}")
+
+
+@pytest.mark.parametrize("qtype", [gs.Q8_0, gs.Q4_0, gs.Q4_K, gs.Q6_K])
+def test_one_token_layer_with_edge_blocks(qg, oracle_lib, qtype):
+    """Edge-value blocks (code -128, negative / subnormal / extreme d, zero d or dmin, extreme
+    scales) dealt over every expert's gate, up and down rows: the fused one-token layer still
+    matches the oracle stage by stage."""
+    H, F = SHAPES[qtype]
+    E, k = 16, 4
+    ex = Experts(qtype, E, H, F, seed=90 + qtype)
+    qk, bb = gs.BLOCK[qtype]
+    edge = eb.edge_blocks(qtype)
+    go, uo, do = ex.offs
+    host = ex.host.copy()
+    nb = 0
+    for e in range(E):
+        for base, rows, K in ((go, F, H), (uo, F, H), (do, H, F)):
+            off = e * ex.stride + base
+            blocks = host[off:off + rows * (K // qk) * bb].reshape(-1, bb)
+            for i in range(0, blocks.shape[0], 7):
+                blocks[i] = edge[(i // 7 + e) % len(edge)]
+                nb += 1
+    assert nb > 0
+    ex.host = host
+    ex.dev = to_dev(host, torch)
+    wr = gs.router_weights(E, H, seed=qtype + 3)
+    xn = gs.activations(1, H, seed=qtype, stream=58)
+    x = gs.activations(1, H, seed=qtype, stream=59)
+    ids, wts, act, out = _layer(qg, ex, xn, wr, x, k)
+    assert qg.device_status() == 0
+    i2, w2, lg = _route(qg, xn, wr, k)
+    assert np.array_equal(i2, ids) and np.array_equal(w2, wts)
+    check_route(oracle_lib, xn, wr, k, ids, wts, lg, what=f"edge blocks type {qtype}")
+    check_swiglu(oracle_lib, ex, ids, xn, k, act, what=f"edge blocks type {qtype}")
+    check_combine(oracle_lib, ex, ids, wts, act, x, k, out, what=f"edge blocks type {qtype}")
+
+
+def test_one_workspace_serves_every_token_count(qg, oracle_lib):
+    """One workspace sized for T = 8 serves moe_layer at T = 8, 1, 8, 1, 3 in turn and then the
+    standalone router: the one-token grid-barrier counter and the router tickets sit in a fixed
+    header, so no call's scratch (logits, dn rows) lands on them, and every result still
+    matches the oracle."""
+    H, F, E, k = 512, 96, 16, 4
+    ex = Experts(gs.Q8_0, E, H, F, seed=73)
+    gate, up, down = ex.bases()
+    wr = gs.router_weights(E, H, seed=73)
+    wrd = to_dev(wr, torch)
+    ws = _ws(qg, 8, k, E, H, F)
+    for i, T in enumerate((8, 1, 8, 1, 3)):
+        xn = gs.activations(T, H, seed=i, stream=60)
+        x = gs.activations(T, H, seed=i, stream=61)
+        ids = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+        wts = torch.full((T, k), float("nan"), dtype=torch.float32, device="cuda")
+        act = torch.full((T * k, F), float("nan"), dtype=torch.float32, device="cuda")
+        xd = to_dev(x, torch)
+        qg.moe_layer(gs.Q8_0, to_dev(xn, torch), wrd, gate, up, down, ex.stride, None, E, T, H, F, E, k, ids, wts,
+                     act, xd, ws)
+        torch.cuda.synchronize()
+        assert qg.device_status() == 0, T
+        ids_h, wts_h, act_h, out = ids.cpu().numpy(), wts.cpu().numpy(), act.cpu().numpy(), xd.cpu().numpy()
+        i2, w2, lg = _route(qg, xn, wr, k)
+        assert np.array_equal(i2, ids_h), T
+        check_route(oracle_lib, xn, wr, k, ids_h, wts_h, lg, what=f"shared workspace T={T}")
+        check_swiglu(oracle_lib, ex, ids_h, xn, k, act_h, what=f"shared workspace T={T}")
+        check_combine(oracle_lib, ex, ids_h, wts_h, act_h, x, k, out, what=f"shared workspace T={T}")
+    # the standalone router on the same workspace: its tickets read zero again
+    xn = gs.activations(8, H, seed=9, stream=62)
+    ids = torch.full((8, k), -7, dtype=torch.int32, device="cuda")
+    wts = torch.full((8, k), float("nan"), dtype=torch.float32, device="cuda")
+    qg.moe_route_topk(to_dev(xn, torch), wrd, 8, H, E, k, ids, wts, None, ws)
+    torch.cuda.synchronize()
+    i2, w2, _ = _route(qg, xn, wr, k)
+    assert np.array_equal(ids.cpu().numpy(), i2) and np.array_equal(wts.cpu().numpy(), w2)

@@ -16,6 +16,7 @@ from fractions import Fraction
 import numpy as np
 import pytest
 
+import edge_blocks as eb
 import gguf_synth as gs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_blocks.txt")
@@ -71,6 +72,33 @@ def test_q4_0_hand_blocks(oracle_lib):
     exp = [0.0] * 32
     exp[3], exp[19] = -4.0, 3.5
     assert b.tolist() == exp
+
+
+def test_q8_0_edge_hand_blocks(oracle_lib):
+    """Code 0x80 (-128), a negative d, the smallest subnormal d and the most negative d."""
+    hb = _hand_blocks()
+    e = _vals(oracle_lib, gs.Q8_0, hb["q8_hand_e"][1], 32)
+    assert e.tolist() == [-128.0 if i % 2 == 0 else 127.0 for i in range(32)]
+    f = _vals(oracle_lib, gs.Q8_0, hb["q8_hand_f"][1], 32)
+    assert f.tolist() == [(16 - i) / 2 for i in range(32)]
+    g = _vals(oracle_lib, gs.Q8_0, hb["q8_hand_g"][1], 32)
+    assert g.tolist() == [-(2.0 ** -17)] * 32
+    h = _vals(oracle_lib, gs.Q8_0, hb["q8_hand_h"][1], 32)
+    q = [-128] + [i - 16 for i in range(1, 31)] + [127]
+    assert h.tolist() == [-65504.0 * v for v in q]
+
+
+def test_q4_0_edge_hand_blocks(oracle_lib):
+    """A negative d (ggml's d = max / -8), a subnormal d and the largest finite d."""
+    hb = _hand_blocks()
+    c = _vals(oracle_lib, gs.Q4_0, hb["q4_hand_c"][1], 32)
+    assert c[:16].tolist() == [(j - 7) / 4 for j in range(16)]
+    assert c[16:].tolist() == [(8 - j) / 4 for j in range(16)]
+    d = _vals(oracle_lib, gs.Q4_0, hb["q4_hand_d"][1], 32)
+    assert d[:16].tolist() == [3 * (j - 8) * 2.0 ** -24 for j in range(16)]
+    assert d[16:].tolist() == [3 * (7 - j) * 2.0 ** -24 for j in range(16)]
+    e = _vals(oracle_lib, gs.Q4_0, hb["q4_hand_e"][1], 32)
+    assert e.tolist() == [7 * 65504.0] * 16 + [-8 * 65504.0] * 16
 
 
 def test_q8_q4_products_exact(oracle_lib):
@@ -163,6 +191,28 @@ def test_q4_k_hand_blocks(oracle_lib, case):
     got = _vals(oracle_lib, gs.Q4_K, blk, 256)
     exp = [_round_f32(v) for v in _q4k_closed_form(dbits, dminbits, sc, mn, qs)]
     assert got.tolist() == [float(e) for e in exp]
+
+
+@pytest.mark.parametrize("idx", range(len(eb.Q4K_EDGE)))
+def test_q4_k_edge_blocks(oracle_lib, idx):
+    """d = 0, dmin = 0, all-63 scales and mins, subnormal and negative d, the largest d: the
+    oracle equals the exact d*sc*q - dmin*m rounded once, from the fields."""
+    name, blk, (dbits, dminbits, sc, mn, qs) = eb.q4k_edge_blocks()[idx]
+    got = _vals(oracle_lib, gs.Q4_K, blk, 256)
+    exp = [_round_f32(v) for v in _q4k_closed_form(dbits, dminbits, sc, mn, qs)]
+    assert got.tolist() == [float(v) for v in exp], name
+
+
+@pytest.mark.parametrize("idx", range(len(eb.Q6K_EDGE)))
+def test_q6_k_edge_blocks(oracle_lib, idx):
+    """Scales -32 and 31 with a subnormal, an extreme and a normal d; uniform ql / qh bytes give
+    one 6-bit code per quarter, so w_i = d * sc[i // 16] * (Q[(i % 128) // 32] - 32)."""
+    name, blk, (dbits, sc, ql, qh) = eb.q6k_edge_blocks()[idx]
+    Q = [((ql >> (4 * (qd >> 1))) & 15) | (((qh >> (2 * qd)) & 3) << 4) for qd in range(4)]
+    d = Fraction(_f16(dbits))
+    exp = [d * sc[i // 16] * (Q[(i % 128) // 32] - 32) for i in range(256)]
+    got = _vals(oracle_lib, gs.Q6_K, blk, 256)
+    assert [Fraction(float(v)) for v in got] == exp, name
 
 
 def _scale_min_page(j, sc):
