@@ -253,7 +253,8 @@ def profiled_traffic():
 def kernel_source_hash():
     """Hash of the headline kernel's sources: its translation unit and the headers it includes."""
     csrc = os.path.join(ROOT, "gguf_block_dequant_gb300", "csrc")
-    files = [os.path.join(csrc, f) for f in ("qg_gemv.cu", "qg_decode.cuh", "qg_common.cuh", "qg_pipe.cuh", "qg_host.h")]
+    files = [os.path.join(csrc, f) for f in ("qg_gemv1.cu", "qg_gemv.cu", "qg_decode.cuh", "qg_common.cuh", "qg_pipe.cuh",
+                                              "qg_host.h")]
     files.append(os.path.join(ROOT, "include", "ggufdq.h"))
     h = hashlib.sha256()
     for path in files:
@@ -340,6 +341,7 @@ def run_section(args):
     qg.load()
     hbm, _, _ = peaks()
     stream = torch.cuda.Stream()
+    qg.set_static_weights(args.weights == "static", stream)
     if args.sections == "gemm":
         res = run_gemm(torch, qg, stream, reps=args.steps, warmup=args.warmup)
     elif args.sections == "moe":
@@ -476,7 +478,7 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
-            "roofline": {"bound": "hbm", "kernel": "qgemv_kernel<Q8_0,T=%d>" % T, "achieved": round(achieved, 2),
+            "roofline": {"bound": "hbm", "kernel": ("qgemv1_kernel<Q8_0> (one token)" if T == 1 else "qgemv_kernel<Q8_0,T=%d>" % T), "achieved": round(achieved, 2),
                          "peak": hbm, "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                          "traffic": traffic,
                          "algorithmic_bytes_per_launch": round((wbytes + abytes) / launches, 1)},
