@@ -544,9 +544,9 @@ qg_status launch_cfg(int nmat, const void *const *w, const float *x, float *cons
 template <int QT, int TT>
 qg_status launch_t(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
                    int T, cudaStream_t stream) {
+  const qg_status r = qg::gemv1_launch<QT>(nmat, w, x, y, Ms, N, T, stream);
+  if (r != QG_EUNSUPPORTED) return r;
   if constexpr (TT == 1) {
-    const qg_status r = qg::gemv1_launch<QT>(nmat, w, x, y, Ms, N, stream);
-    if (r != QG_EUNSUPPORTED) return r;
     if constexpr (QT == QG_TYPE_Q4_K) {
       using D = Dec<QT>;
       const long long xres = (N + D::SG - 1) / D::SG * D::SG * 4;

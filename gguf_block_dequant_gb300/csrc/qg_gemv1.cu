@@ -47,6 +47,8 @@ struct G1Args {
   int NS;
   int max_kw;
   int N;
+  int T;                 // token columns (<= TT of the kernel)
+  uint32_t xtok;         // shared-memory bytes of one token's activations
   int xR, box_rows;
   uint32_t off_x, off_red, off_ring;
   int early_weights;
@@ -54,15 +56,19 @@ struct G1Args {
 
 QG_DEVICE void g1_status(unsigned int bits) { atomicOr(&g_qg_status_gemv, bits); }
 
-// QT block type, NW warps per CTA, CPS CTAs per SM, RR rows per row block
-template <int QT, int NW, int CPS, int RR>
+// QT block type, NW warps per CTA, CPS CTAs per SM, RR rows per row block, GU groups per
+// chunk when known at compile time (0: a runtime loop), TT token columns (a.T <= TT of them
+// are used).  With GU the group loop is unrolled: every group's shared-memory offsets become
+// immediates of the loads.  One token takes the fused dot (Dec::dot1); several tokens decode
+// each weight once and multiply it into every token column.
+template <int QT, int NW, int CPS, int RR, int GU, int TT>
 __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_constant__ CUtensorMap xmap, const G1Args a) {
   using D = Dec<QT>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *wbar = reinterpret_cast<uint64_t *>(smem);  // [NW][kNS]
   uint64_t *xfull = wbar + NW * kNS;
-  float *red = reinterpret_cast<float *>(smem + a.off_red);  // [NW][RR] (K-split partial sums)
+  float *red = reinterpret_cast<float *>(smem + a.off_red);  // [NW][RR * TT] (K-split partial sums)
   uint8_t *xs = smem + a.off_x;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -143,7 +149,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
   if (a.early_weights) prologue();
   pdl_wait();
   pdl_launch_dependents();
-  if (threadIdx.x == 0) load_x(xs, &xmap, 1, a.N, 0, a.xR, a.box_rows, xfull);
+  if (threadIdx.x == 0) load_x(xs, &xmap, a.T, a.N, 0, a.xR, a.box_rows, xfull);
   if (!a.early_weights) prologue();
 
   const uint32_t wo = static_cast<uint32_t>(D::woff(lane));
@@ -155,6 +161,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
 
   bool ok = mbar_wait(xfull, 0);
   float acc[RR];
+  f2 acc2[RR][TT];
   int ci = 0, i = 0, cs = 0, done = 0;
   uint32_t phase = 0;
   for (int t = 0; t < items; ++t) {
@@ -165,7 +172,11 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
     const int c = kw + ci * KW;
     if (ci == 0) {
 #pragma unroll
-      for (int r = 0; r < RR; ++r) acc[r] = 0.f;
+      for (int r = 0; r < RR; ++r) {
+        acc[r] = 0.f;
+#pragma unroll
+        for (int t = 0; t < TT; ++t) acc2[r][t] = mk2(0.f, 0.f);
+      }
     }
     if (ok && !mbar_wait(&mybar[cs], phase)) ok = false;
     if (ok) {
@@ -179,17 +190,47 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
       auto group = [&](int g) {
         const uint32_t goff = static_cast<uint32_t>(g * D::GB);
         const uint32_t xg = xg0 + static_cast<uint32_t>(g * (D::SG * 4));
-        float4 xc[D::NCH];
-#pragma unroll
-        for (int ch = 0; ch < D::NCH; ++ch) xc[ch] = lds_f4(xg + xo[ch]);
-        const float aux = D::xaux(xc);
         typename D::U u[RR];
+        if constexpr (TT == 1) {
+          float4 xc[D::NCH];
 #pragma unroll
-        for (int r = 0; r < RR; ++r) u[r] = rp[r].load(goff, lane);
+          for (int ch = 0; ch < D::NCH; ++ch) xc[ch] = lds_f4(xg + xo[ch]);
+          const float aux = D::xaux(xc);
 #pragma unroll
-        for (int r = 0; r < RR; ++r) acc[r] += D::dot1(u[r], xc, aux);
+          for (int r = 0; r < RR; ++r) u[r] = rp[r].load(goff, lane);
+#pragma unroll
+          for (int r = 0; r < RR; ++r) acc[r] += D::dot1(u[r], xc, aux);
+        } else {
+#pragma unroll
+          for (int r = 0; r < RR; ++r) u[r] = rp[r].load(goff, lane);
+#pragma unroll
+          for (int ch = 0; ch < D::NCH; ++ch) {
+            f2 w01[RR], w23[RR];
+#pragma unroll
+            for (int r = 0; r < RR; ++r) D::weights(u[r], ch, w01[r], w23[r]);
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+              if (t < a.T) {
+                const float4 xv = lds_f4(xg + static_cast<uint32_t>(t) * a.xtok + xo[ch]);
+                const f2 x01 = mk2(xv.x, xv.y), x23 = mk2(xv.z, xv.w);
+#pragma unroll
+                for (int r = 0; r < RR; ++r) {
+                  acc2[r][t] = fma2(w01[r], x01, acc2[r][t]);
+                  acc2[r][t] = fma2(w23[r], x23, acc2[r][t]);
+                }
+              }
+            }
+          }
+        }
       };
-      if (c < nc - 1) {
+      if constexpr (GU > 0) {
+        // a chunk has GU groups, the last one gtail (<= GU); a partial group only at the end
+        const int gl = (c < nc - 1) ? GU : (a.last_full ? a.gtail : a.gtail - 1);
+#pragma unroll
+        for (int g = 0; g < GU; ++g)
+          if (g < gl) group(g);
+        if (c == nc - 1 && !a.last_full && gl * D::SG + bfirst < a.N - c * a.gpc * D::SG) group(gl);
+      } else if (c < nc - 1) {
         for (int g = 0; g < a.gpc; ++g) group(g);
       } else {
         const int gl = a.last_full ? a.gtail : a.gtail - 1;
@@ -203,27 +244,35 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
       phase ^= 1u;
     }
     if (++ci == my_c) {
-      // row block done: the RR row sums, reduce-scattered over the warp
-      float v[RR];
+      // row block done: the RR x TT sums (row r, token t at r * TT + t), reduce-scattered over
+      // the warp so that each lane owns one of them
+      constexpr int NV = RR * TT;
+      static_assert(NV <= 32, "one sum per lane");
+      float v[NV];
 #pragma unroll
-      for (int r = 0; r < RR; ++r) v[r] = acc[r];
-      reduce_scatter<RR>(v, lane);
-      const int r0 = rs_index<RR>(lane);
-      const bool own = rs_owner<RR>(lane);
+      for (int r = 0; r < RR; ++r)
+#pragma unroll
+        for (int t = 0; t < TT; ++t) v[r * TT + t] = (TT == 1) ? acc[r] : acc2[r][t].x + acc2[r][t].y;
+      reduce_scatter<NV>(v, lane);
+      const int i0 = rs_index<NV>(lane);
+      const bool own = rs_owner<NV>(lane);
+      const int r0 = i0 / TT, t0 = i0 - r0 * TT;
       const uint32_t rb = rbA + static_cast<uint32_t>(rbl + i * lanes_rb);
       int j;
       uint32_t row;
       locate(rb, j, row);
+      const uint32_t M = a.M[j];
       if (KW == 1) {
-        if (own && ok && row + r0 < a.M[j]) a.y[j][row + r0] = v[0];
+        if (own && ok && t0 < a.T && row + r0 < M) a.y[j][static_cast<size_t>(t0) * M + row + r0] = v[0];
       } else {
-        float *myred = red + warp * RR;
-        if (own) myred[r0] = v[0];
+        float *myred = red + warp * NV;
+        if (own) myred[i0] = v[0];
         named_bar_sync(1 + rbl, KW * 32);
-        if (kw == 0 && lane < RR) {
+        if (kw == 0 && lane < NV) {
           float s = 0.f;
-          for (int q = 0; q < KW; ++q) s += red[(rbl * KW + q) * RR + lane];
-          if (ok && row + lane < a.M[j]) a.y[j][row + lane] = s;
+          for (int q = 0; q < KW; ++q) s += red[(rbl * KW + q) * NV + lane];
+          const int rr = lane / TT, tt = lane - rr * TT;
+          if (ok && tt < a.T && row + rr < M) a.y[j][static_cast<size_t>(tt) * M + row + rr] = s;
         }
         named_bar_sync(1 + rbl, KW * 32);  // red is reused by the next row block
       }
@@ -243,21 +292,29 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
 
 namespace qg {
 
-// Plans and launches the lean one-token kernel in one CTA shape; QG_EUNSUPPORTED (nothing
-// launched) when the shape is outside its scope, so the caller takes the general kernel.
-template <int QT, int NW, int CPS, int RR>
-qg_status gemv1_cfg(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
-                    cudaStream_t stream) {
+struct G1Plan {
+  G1Args a;
+  CUtensorMap map;
+  unsigned grid;
+  uint32_t smem;
+};
+
+// Plans the lean one-token kernel in one CTA shape; QG_EUNSUPPORTED when the shape is outside
+// its scope (the caller then takes the general kernel).  Enqueues nothing.
+template <int QT, int NW, int CPS, int RR, int TT>
+qg_status gemv1_plan(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
+                     int T, cudaStream_t stream, G1Plan &P) {
   using D = Dec<QT>;
   const DeviceInfo &dev = device_info();
   if (!dev.ok) return QG_ECUDA;
   const long long row_bytes = N / D::QK * D::BB;
   if (row_bytes % 16 != 0) return QG_EUNSUPPORTED;
   const int ngroups = static_cast<int>((N + D::SG - 1) / D::SG);
-  const long long xres = ((static_cast<long long>(ngroups) * D::SG * 4 + 1023) / 1024) * 1024;
+  const long long xtok = static_cast<long long>(ngroups) * D::SG * 4;
+  const long long xres = ((static_cast<long long>(T) * xtok + 1023) / 1024) * 1024;
   const long long budget = (CPS == 1 ? dev.smem_optin : dev.smem_per_sm / CPS) - 4096;
   const uint32_t hdr = 1024;
-  const uint32_t red_bytes = NW * RR * 4;
+  const uint32_t red_bytes = NW * RR * TT * 4;
   G1Args a{};
   unsigned long long rblocks = 0;
   for (int j = 0; j < nmat; ++j) {
@@ -326,35 +383,77 @@ qg_status gemv1_cfg(int nmat, const void *const *w, const float *x, float *const
   a.NS = NS;
   a.max_kw = nchunks;
   a.N = static_cast<int>(N);
+  a.T = T;
+  a.xtok = static_cast<uint32_t>(xtok);
   a.xR = ngroups * D::SG / 32;
   a.box_rows = box_rows_for(a.xR);
   a.off_red = hdr;
   a.off_x = (hdr + red_bytes + 1023) & ~1023u;
   a.off_ring = a.off_x + static_cast<uint32_t>(xres);
   const uint32_t smem = a.off_ring + static_cast<uint32_t>(NW * NS * stage) + 1024;
-  CUtensorMap map;
-  if (!encode_x_map(&map, x, 1, N, a.box_rows)) return QG_ECUDA;
-  auto kern = qgemv1_kernel<QT, NW, CPS, RR>;
-  if (!set_smem_attr(reinterpret_cast<const void *>(kern), smem)) return QG_ECUDA;
+  if (!encode_x_map(&P.map, x, T, N, a.box_rows)) return QG_ECUDA;
   a.early_weights = static_weights(stream) ? 1 : 0;
-  if (launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(NW * 32), smem, stream, map, a) != cudaSuccess)
-    return QG_ECUDA;
+  P.a = a;
+  P.grid = static_cast<unsigned>(grid);
+  P.smem = smem;
+  return QG_OK;
+}
+
+template <int QT, int NW, int CPS, int RR, int GU, int TT>
+qg_status gemv1_run(const G1Plan &P, cudaStream_t stream) {
+  auto kern = qgemv1_kernel<QT, NW, CPS, RR, GU, TT>;
+  if (!set_smem_attr(reinterpret_cast<const void *>(kern), P.smem)) return QG_ECUDA;
+  if (launch_pdl(kern, dim3(P.grid), dim3(NW * 32), P.smem, stream, P.map, P.a) != cudaSuccess) return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
 
+// One CTA shape, its group loop unrolled for the chunk sizes of the common row lengths
+// (2560 -> 5 groups, 4096 and 9728 -> chunks of 4, 1024 -> 2), a runtime loop otherwise.
+template <int QT, int NW, int CPS, int RR, int TT>
+qg_status gemv1_cfg(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
+                    int T, cudaStream_t stream) {
+  G1Plan P;
+  const qg_status r = gemv1_plan<QT, NW, CPS, RR, TT>(nmat, w, x, y, Ms, N, T, stream, P);
+  if (r != QG_OK) return r;
+  if constexpr (TT == 1) {
+    switch (P.a.gpc) {
+      case 5: return gemv1_run<QT, NW, CPS, RR, 5, TT>(P, stream);
+      case 4: return gemv1_run<QT, NW, CPS, RR, 4, TT>(P, stream);
+      case 2: return gemv1_run<QT, NW, CPS, RR, 2, TT>(P, stream);
+      default: break;
+    }
+  }
+  return gemv1_run<QT, NW, CPS, RR, 0, TT>(P, stream);
+}
+
+// CTA shape per token count: two 8-warp CTAs per SM while the activations leave them room,
+// else one 8-warp CTA per SM (more shared memory and registers per warp).
 template <int QT>
 qg_status gemv1_launch(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
-                       cudaStream_t stream) {
-  return gemv1_cfg<QT, 8, 2, 2>(nmat, w, x, y, Ms, N, stream);
+                       int T, cudaStream_t stream) {
+  if (T == 1) return gemv1_cfg<QT, 8, 2, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
+  // several tokens: the 32-element types (the K-quants' lane state is too large to keep TT
+  // accumulators beside it; they take the general kernel)
+  if constexpr (QT != QG_TYPE_Q8_0 && QT != QG_TYPE_Q4_0) {
+    return QG_EUNSUPPORTED;
+  } else {
+    qg_status r = QG_EUNSUPPORTED;
+    if (T == 2) r = gemv1_cfg<QT, 8, 2, 2, 2>(nmat, w, x, y, Ms, N, T, stream);
+    else if (T <= 4) r = gemv1_cfg<QT, 8, 2, 2, 4>(nmat, w, x, y, Ms, N, T, stream);
+    if (r != QG_EUNSUPPORTED || T <= 2) return r;
+    if (T <= 4) return gemv1_cfg<QT, 8, 1, 2, 4>(nmat, w, x, y, Ms, N, T, stream);
+    if (T <= 8) return gemv1_cfg<QT, 8, 1, 2, 8>(nmat, w, x, y, Ms, N, T, stream);
+    return gemv1_cfg<QT, 8, 1, 2, 16>(nmat, w, x, y, Ms, N, T, stream);
+  }
 }
 
 template qg_status gemv1_launch<QG_TYPE_Q8_0>(int, const void *const *, const float *, float *const *, const int64_t *,
-                                              int64_t, cudaStream_t);
+                                              int64_t, int, cudaStream_t);
 template qg_status gemv1_launch<QG_TYPE_Q4_0>(int, const void *const *, const float *, float *const *, const int64_t *,
-                                              int64_t, cudaStream_t);
+                                              int64_t, int, cudaStream_t);
 template qg_status gemv1_launch<QG_TYPE_Q4_K>(int, const void *const *, const float *, float *const *, const int64_t *,
-                                              int64_t, cudaStream_t);
+                                              int64_t, int, cudaStream_t);
 template qg_status gemv1_launch<QG_TYPE_Q6_K>(int, const void *const *, const float *, float *const *, const int64_t *,
-                                              int64_t, cudaStream_t);
+                                              int64_t, int, cudaStream_t);
 
 }  // namespace qg

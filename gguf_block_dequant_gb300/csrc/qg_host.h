@@ -67,11 +67,11 @@ qg_status moe_combine_tc(const void *w_down, int64_t stride, const int32_t *slot
                          const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
                          float *x_inout, int add_residual, float *dn, void *ws, cudaStream_t s);
 
-// one-token GEMV, lean kernel for rows of 16-byte multiples with resident activations
-// (qg_gemv1.cu); QG_EUNSUPPORTED with nothing launched for other shapes
+// GEMV over T <= 16 token columns, lean kernel for rows of 16-byte multiples with resident
+// activations (qg_gemv1.cu); QG_EUNSUPPORTED with nothing launched for other shapes
 template <int QT>
 qg_status gemv1_launch(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
-                       cudaStream_t stream);
+                       int T, cudaStream_t stream);
 
 qg_status gemv_multi_dispatch(int type, int n, const void *const *w, const float *x, float *const *y,
                               const int64_t *M, int64_t N, int T, cudaStream_t s);

@@ -802,14 +802,24 @@ struct OneArgs {
   float *wts_out;
   float *act;        // [k][F]
   float *x;          // [H], updated in place
-  float *logits;     // [E] (workspace)
-  unsigned long long *bar;  // arrivals of the grid barriers (workspace, 8-byte aligned)
+  unsigned long long *bar;   // arrivals of the grid barrier (workspace header)
+  unsigned long long *gen;   // calls of this kernel on the workspace (header; tags the logits)
+  unsigned long long *xlog;  // [E] logits, each tagged with its call (header)
   long long rbh, rbf;  // bytes of an H-long row (gate, up) and of an F-long row (down)
   int NS, stage_bytes, gseg, dseg;
   int hmax;          // most hidden rows of one CTA
   int early_weights;
   uint32_t off_x, off_part, off_ring;
 };
+
+QG_DEVICE unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+QG_DEVICE void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
 QG_DEVICE void prefetch_l2(uintptr_t p, uint32_t n) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
@@ -819,7 +829,9 @@ QG_DEVICE void prefetch_l2(uintptr_t p, uint32_t n) {
 // launch adds exactly G per barrier and launches in a stream do not overlap this part (it comes
 // after the wait on the predecessor), so the arrivals of one barrier all return values in
 // [n G, n G + G) for the same n, and the barrier is passed once the count reaches (n + 1) G.
-// Returns false when the wait expired.
+// The arrival follows a fence (this CTA's writes before it); the polls are acquire loads, so
+// what the other CTAs wrote before arriving is visible after the barrier.  Returns false when
+// the wait expired.
 QG_DEVICE bool grid_barrier(unsigned long long *bar, unsigned int nctas, unsigned int *s_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -828,13 +840,15 @@ QG_DEVICE bool grid_barrier(unsigned long long *bar, unsigned int nctas, unsigne
     const unsigned long long target = (v / nctas + 1) * nctas;
     unsigned int ok = 1u;
     const uint64_t t0 = global_ns();
-    while (*reinterpret_cast<volatile unsigned long long *>(bar) < target) {
-      if (global_ns() - t0 > QG_WAIT_NS) {
+    for (unsigned int spin = 1;; ++spin) {
+      unsigned long long cur;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(cur) : "l"(bar) : "memory");
+      if (cur >= target) break;
+      if ((spin & 31u) == 0u && global_ns() - t0 > QG_WAIT_NS) {
         ok = 0u;
         break;
       }
     }
-    __threadfence();
     *s_flag = ok;
   }
   __syncthreads();
@@ -852,7 +866,8 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
   int32_t *s_slot = reinterpret_cast<int32_t *>(smem + 768);           // [kMaxK] slot, -1: bad id
   int32_t *s_vz = reinterpret_cast<int32_t *>(smem + 896);             // [kMaxK] valid picks in order
   float *red = reinterpret_cast<float *>(smem + 1024);                 // [NW] router partials
-  unsigned int *s_misc = reinterpret_cast<unsigned int *>(smem + 1024 + 4 * NW);  // flag, valid count
+  unsigned int *s_misc = reinterpret_cast<unsigned int *>(smem + 1024 + 4 * NW);  // flag, valid count, tag
+  uintptr_t *s_base = reinterpret_cast<uintptr_t *>(smem + 1152);      // [kMaxK][3] gate, up, down of valid picks
   uint8_t *xs = smem + a.off_x;
   float *part = reinterpret_cast<float *>(smem + a.off_part);          // [hmax][kMaxK]
   uint8_t *ring = smem + a.off_ring;
@@ -868,8 +883,15 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
 
   // ---- phase 0: router logits of experts blockIdx.x, + G, ..., summed by kRouterWarps warps
   // in exactly the order of moe_router_kernel, so that the logits (and picks and weights) are
-  // the ones the standalone router gives
+  // the ones the standalone router gives.  Each logit is published as one 64-bit word holding
+  // this call's tag and the value, so every CTA can gather all of them without a grid barrier:
+  // a word carrying the tag is this call's logit.  The tag is the number of earlier calls on
+  // the workspace plus one (CTA 0 advances the count once every CTA is past the grid barrier,
+  // so every CTA of a call reads the same count).
   pdl_wait();
+  if (threadIdx.x == 0) s_misc[2] = static_cast<unsigned int>(ld_relaxed_u64(a.gen)) + 1u;
+  __syncthreads();
+  const unsigned int tag = s_misc[2];
   bool ok = true;
   const int H4 = H >> 2;
   for (int e = blockIdx.x; e < a.E; e += G) {
@@ -894,20 +916,31 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
       float t = 0.f;
 #pragma unroll
       for (int w = 0; w < kRouterWarps; ++w) t += red[w];
-      a.logits[e] = t;
+      st_relaxed_u64(a.xlog + e, (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(t));
     }
     __syncthreads();
   }
-  // the token's activations into shared memory (128-byte swizzled rows) while the grid meets
+  // the token's activations into shared memory (128-byte swizzled rows) while the logits arrive
   copy_x_row(xs, 0, 0, a.xn, H, threadIdx.x, NW * 32);
-  if (!grid_barrier(a.bar, static_cast<unsigned int>(G), s_misc)) ok = false;
 
   // ---- phase 1: picks, then the gate/up row pairs.  The k greedy picks of the logits (ties
   // to the lowest expert id) are the experts of rank < k, rank(e) = #{e' : l[e'] > l[e] or
   // l[e'] == l[e] and e' < e}; the weights follow in pick order as in topk_token.
   float *s_l = part;  // the logits (part is free until phase 2)
-  for (int e = threadIdx.x; e < a.E; e += NW * 32) s_l[e] = __ldcg(a.logits + e);
-  __syncthreads();
+  int late = 0;
+  for (int e = threadIdx.x; e < a.E; e += NW * 32) {
+    // bounded wait for this call's tag on expert e's word
+    unsigned long long v = ld_relaxed_u64(a.xlog + e);
+    if (static_cast<unsigned int>(v >> 32) != tag) {
+      const uint64_t t0 = global_ns();
+      do {
+        v = ld_relaxed_u64(a.xlog + e);
+      } while (static_cast<unsigned int>(v >> 32) != tag && global_ns() - t0 < QG_WAIT_NS);
+      if (static_cast<unsigned int>(v >> 32) != tag) late = 1;
+    }
+    s_l[e] = __uint_as_float(static_cast<unsigned int>(v));
+  }
+  if (__syncthreads_or(late)) ok = false;
   {
     // rank(e) in four partial counts over quarters of the experts, so that every warp of the
     // CTA takes a share (the ring is idle until the gate/up stages: it holds the counts)
@@ -959,6 +992,14 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
     const unsigned int m = __ballot_sync(0xFFFFFFFFu, valid);
     if (valid) s_vz[__popc(m & ((1u << lane) - 1u))] = lane;
     if (lane == 0) s_misc[1] = __popc(m);
+    __syncwarp();
+    // the valid picks' expert bases (gate, up and down rows of slot s_slot)
+    if (lane < static_cast<int>(__popc(m))) {
+      const uintptr_t off = static_cast<uintptr_t>(s_slot[s_vz[lane]]) * static_cast<uintptr_t>(a.stride);
+      s_base[3 * lane + 0] = reinterpret_cast<uintptr_t>(a.wg) + off;
+      s_base[3 * lane + 1] = reinterpret_cast<uintptr_t>(a.wu) + off;
+      s_base[3 * lane + 2] = reinterpret_cast<uintptr_t>(a.wd) + off;
+    }
   }
   cp_async_wait_all();
   __syncthreads();
@@ -992,139 +1033,150 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
   uint8_t *wring = ring + warp * a.NS * a.stage_bytes;
   const uint32_t wring_s = smem_u32(wring);
   const uint32_t xs_s = smem_u32(xs);
+  const int bfirst = D::block_first(lane);
 
-  // up to 4 rows against activation row xrow: the dense one-token decode
-  auto dot_rows = [&](const uint32_t (&wrow)[4], int nrows, int K, uint32_t xrow, float (&acc)[4]) {
+  // RR rows of one stage against activation row xrow: the dense one-token decode, row r's
+  // raw blocks at shared address row[r] (any 2-byte alignment), K elements
+  auto dot_rows = [&](auto &acc, const uint32_t *row, int K, uint32_t xrow) {
+    constexpr int RR = static_cast<int>(sizeof(acc) / sizeof(acc[0]));
+    RowPrep<QT> rp[RR];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) acc[r] = 0.f;
-    const int gcount = (K + D::SG - 1) / D::SG;
-    for (int g = 0; g < gcount; ++g) {
-      if (g * D::SG + D::block_first(lane) >= K) break;
+    for (int r = 0; r < RR; ++r) {
+      acc[r] = 0.f;
+      rp[r].init(row[r] + wo, lane);
+    }
+    auto group = [&](int g) {
       const uint32_t goff = static_cast<uint32_t>(g * D::GB);
       const uint32_t xg = xrow + static_cast<uint32_t>(g * (D::SG * 4));
       float4 xc[D::NCH];
 #pragma unroll
       for (int ch = 0; ch < D::NCH; ++ch) xc[ch] = lds_f4(xg + xo[ch]);
       const float aux = D::xaux(xc);
+      typename D::U w[RR];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-        if (r < nrows) {
-          typename D::U w = D::load(wrow[r] + goff, lane);
-          acc[r] += D::dot1(w, xc, aux);
-        }
-    }
+      for (int r = 0; r < RR; ++r) w[r] = rp[r].load(goff, lane);
+#pragma unroll
+      for (int r = 0; r < RR; ++r) acc[r] += D::dot1(w[r], xc, aux);
+    };
+    const int gfull = K / D::SG;
+    for (int g = 0; g < gfull; ++g) group(g);
+    if (gfull * D::SG < K && gfull * D::SG + bfirst < K) group(gfull);  // the partial last group
   };
 
-  // Streaming of this warp's items through its ring.  Ring positions continue across the
-  // phases, so every slot's mbarrier phase stays in step.  describe(item, r, src, n, mend)
-  // gives row r (< 8) of an item's stage (n = 0: none), stored at r * row_stride in the slot;
-  // consume(item, stage address) computes it.  After an expired wait the warp issues nothing
-  // more and waits for what it has in flight before it exits.
-  int issued = 0, waited = 0, ph_base = 0, ph_n = 0;
+  // Streaming through the warp's ring.  Ring positions continue across the phases, so every
+  // slot's mbarrier phase stays in step: `issued` copies were requested, `waited` consumed.
+  // After an expired wait the warp issues nothing more and waits for what it has in flight
+  // before it exits.
+  int issued = 0, waited = 0;
   int islot = 0, wslot = 0, wph = 0;  // ring slot of the next issue / wait, and the wait's phase bit
-  auto issue_next = [&](auto &&describe, int row_stride) {
-    uintptr_t src = 0, mend = 0;
-    uint32_t n = 0;
-    if (lane < 8) describe(issued - ph_base, lane, src, n, mend);
-    uint8_t *dst = wring + islot * a.stage_bytes + lane * row_stride;
-    warp_bulk_copies(dst, src, n, mend, &wbar[warp * kMaxNS + islot], lane);
+  auto next_slot = [&]() {
     ++issued;
     if (++islot == a.NS) islot = 0;
   };
-  // begin issues up to `ahead` stages: NS - 1 (the next one is issued before each wait, into
-  // the slot consumed last) or NS (a full ring; each slot is refilled right after it is
-  // consumed)
-  int ph_ahead = 0;
-  auto begin = [&](int n_items, auto &&describe, int row_stride, int ahead) {
-    ph_base = issued;
-    ph_n = n_items;
-    ph_ahead = ahead;
-    while (ok && issued - ph_base < n_items && issued - ph_base < ahead) issue_next(describe, row_stride);
+  auto wait_slot = [&]() {
+    if (!mbar_wait(&wbar[warp * kMaxNS + wslot], static_cast<uint32_t>(wph))) return false;
+    return true;
   };
-  auto finish = [&](auto &&describe, int row_stride, auto &&consume) {
-    const bool full = ph_ahead == a.NS;
-    // positions are waited for in order across the phases: waited == ph_base + it here
-    for (int it = 0; it < ph_n && ok; ++it) {
-      if (!full && issued - ph_base < ph_n) issue_next(describe, row_stride);
-      if (!mbar_wait(&wbar[warp * kMaxNS + wslot], static_cast<uint32_t>(wph))) {
-        ok = false;
-        break;
-      }
-      consume(it, wring_s + static_cast<uint32_t>(wslot * a.stage_bytes));
-      __syncwarp();  // every lane is done with the slot before it is refilled
-      ++waited;
-      if (++wslot == a.NS) {
-        wslot = 0;
-        wph ^= 1;
-      }
-      if (full && issued - ph_base < ph_n) issue_next(describe, row_stride);
+  auto release_slot = [&]() {
+    __syncwarp();  // every lane is done with the slot before it is refilled
+    ++waited;
+    if (++wslot == a.NS) {
+      wslot = 0;
+      wph ^= 1;
     }
   };
 
-  // gate/up: row pairs (pick jv, row i), contiguous balanced ranges per CTA; stage row 0 is the
-  // gate row, row 1 the up row
+  // gate/up: row pairs (pick jv, row i), contiguous balanced ranges per CTA, the warp's pairs
+  // NW apart; a stage holds the gate row (lane 0's copy) and the up row (lane 1's copy, at
+  // gseg).  Cursors advance by NW rows, with no division in the loop.
   {
     const long long nb = static_cast<long long>(kv) * F;
     const int bA = static_cast<int>(static_cast<long long>(blockIdx.x) * nb / G);
     const int bB = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * nb / G);
     const int nrb = bB - bA;
     const int n_items = warp < nrb ? (nrb - warp + NW - 1) / NW : 0;
-    auto pair_of = [&](int item, int &jv, int &i) {  // kv * F < 2^31 (kv <= 32 picks)
-      const int b = bA + warp + item * NW;
-      jv = b / F;
-      i = b - jv * F;
+    int jvi = (bA + warp) / F, ii = (bA + warp) - jvi * F;  // issue cursor
+    int jvc = jvi, ic = ii;                                   // consume cursor
+    auto adv = [&](int &jv, int &i) {
+      i += NW;
+      while (i >= F) {
+        i -= F;
+        ++jv;
+      }
     };
     auto row_src = [&](int jv, int i, int r) {
-      return reinterpret_cast<uintptr_t>(r == 0 ? a.wg : a.wu) +
-             static_cast<uintptr_t>(s_slot[s_vz[jv]]) * static_cast<uintptr_t>(a.stride) +
-             static_cast<uintptr_t>(i) * static_cast<uintptr_t>(a.rbh);
+      return s_base[3 * jv + r] + static_cast<uintptr_t>(i) * static_cast<uintptr_t>(a.rbh);
     };
-    auto describe = [&](int item, int r, uintptr_t &src, uint32_t &n, uintptr_t &mend) {
-      if (r > 1) return;
-      int jv, i;
-      pair_of(item, jv, i);
-      src = row_src(jv, i, r);
-      n = static_cast<uint32_t>(a.rbh);
-      mend = r == 0 ? a.mend_g : a.mend_u;
+    auto issue = [&]() {
+      uintptr_t src = 0, mend = 0;
+      uint32_t n = 0;
+      if (lane < 2) {
+        src = row_src(jvi, ii, lane);
+        n = static_cast<uint32_t>(a.rbh);
+        mend = lane ? a.mend_u : a.mend_g;
+      }
+      warp_bulk_copies(wring + islot * a.stage_bytes + lane * a.gseg, src, n, mend, &wbar[warp * kMaxNS + islot], lane);
+      next_slot();
+      adv(jvi, ii);
     };
-    begin(n_items, describe, a.gseg, a.NS - 1);
-    finish(describe, a.gseg, [&](int item, uint32_t st) {
-      int jv, i;
-      pair_of(item, jv, i);
-      const uint32_t wrow[4] = {st + (static_cast<uint32_t>(row_src(jv, i, 0)) & 15u) + wo,
-                                st + static_cast<uint32_t>(a.gseg) + (static_cast<uint32_t>(row_src(jv, i, 1)) & 15u) + wo,
-                                0u, 0u};
-      float acc[4];
-      dot_rows(wrow, 2, H, xs_s, acc);
-      const float gsum = warp_sum(acc[0]), usum = warp_sum(acc[1]);
-      if (lane == 0) a.act[static_cast<size_t>(s_vz[jv]) * F + i] = silu_mul(gsum, usum);
-    });
+    int n_iss = 0;
+    for (; ok && n_iss < n_items && n_iss < a.NS - 1; ++n_iss) issue();
+    for (int it = 0; it < n_items && ok; ++it) {
+      if (n_iss < n_items) {
+        issue();
+        ++n_iss;
+      }
+      if (!wait_slot()) {
+        ok = false;
+        break;
+      }
+      const uint32_t st = wring_s + static_cast<uint32_t>(wslot * a.stage_bytes);
+      const uint32_t rows[2] = {st + (static_cast<uint32_t>(row_src(jvc, ic, 0)) & 15u),
+                                st + static_cast<uint32_t>(a.gseg) + (static_cast<uint32_t>(row_src(jvc, ic, 1)) & 15u)};
+      float acc[2];
+      dot_rows(acc, rows, H, xs_s);
+      // gate sum to lane 0, up sum to lane 16, then the up sum to lane 0 for the SwiGLU
+      reduce_scatter<2>(acc, lane);
+      const float usum = __shfl_sync(0xFFFFFFFFu, acc[0], 16);
+      if (lane == 0) a.act[static_cast<size_t>(s_vz[jvc]) * F + ic] = silu_mul(acc[0], usum);
+      release_slot();
+      adv(jvc, ic);
+    }
   }
 
   // down: items (pick jv, 4 consecutive hidden rows of this CTA), one copy of the rows (they
-  // are contiguous); their first stages are requested before the barrier (the rows are known)
+  // are contiguous); the ring is filled before the grid barrier (the rows are known), each
+  // slot refilled right after it is consumed
   const int nh = hB - hA, nqd = (nh + 3) / 4;
   const int n2 = warp < kv * nqd ? (kv * nqd - warp + NW - 1) / NW : 0;
-  auto item2 = [&](int item, int &jv, int &h0, int &nr) {
-    const int u = warp + item * NW;
-    jv = u / nqd;
-    h0 = 4 * (u - jv * nqd);
-    nr = min(4, nh - h0);
+  int jd_i = nqd > 0 ? warp / nqd : 0, qd_i = warp - jd_i * nqd;  // issue cursor (quad qd of pick jd)
+  int jd_c = jd_i, qd_c = qd_i;                                     // consume cursor
+  auto adv2 = [&](int &jv, int &q) {
+    q += NW;
+    while (q >= nqd) {
+      q -= nqd;
+      ++jv;
+    }
   };
-  auto down_src = [&](int jv, int hl) {
-    return reinterpret_cast<uintptr_t>(a.wd) + static_cast<uintptr_t>(s_slot[s_vz[jv]]) * static_cast<uintptr_t>(a.stride) +
-           static_cast<uintptr_t>(hA + hl) * static_cast<uintptr_t>(a.rbf);
+  auto down_src = [&](int jv, int q) {
+    return s_base[3 * jv + 2] + static_cast<uintptr_t>(hA + 4 * q) * static_cast<uintptr_t>(a.rbf);
   };
-  auto describe2 = [&](int item, int r, uintptr_t &src, uint32_t &n, uintptr_t &mend) {
-    if (r != 0) return;
-    int jv, h0, nr;
-    item2(item, jv, h0, nr);
-    src = down_src(jv, h0);
-    n = static_cast<uint32_t>(nr) * static_cast<uint32_t>(a.rbf);
-    mend = a.mend_d;
+  auto issue2 = [&]() {
+    uintptr_t src = 0;
+    uint32_t n = 0;
+    if (lane == 0) {
+      src = down_src(jd_i, qd_i);
+      n = static_cast<uint32_t>(min(4, nh - 4 * qd_i)) * static_cast<uint32_t>(a.rbf);
+    }
+    warp_bulk_copies(wring + islot * a.stage_bytes, src, n, a.mend_d, &wbar[warp * kMaxNS + islot], lane);
+    next_slot();
+    adv2(jd_i, qd_i);
   };
-  begin(n2, describe2, a.dseg, a.NS);
+  int n2_iss = 0;
+  for (; ok && n2_iss < n2 && n2_iss < a.NS; ++n2_iss) issue2();
   if (!grid_barrier(a.bar, static_cast<unsigned int>(G), s_misc)) ok = false;
+  // every CTA has read the call count: advance it for the next call on this workspace
+  if (blockIdx.x == 0 && threadIdx.x == 0) st_relaxed_u64(a.gen, tag);
   pdl_launch_dependents();
 
   // ---- phase 2: the act rows of the valid picks into shared memory, the down dots, and the
@@ -1133,20 +1185,27 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
   for (int jv = 0; jv < kv; ++jv) copy_x_row(xs, jv, xrow_f, a.act + static_cast<size_t>(s_vz[jv]) * F, F, threadIdx.x, NW * 32);
   cp_async_wait_all();
   __syncthreads();
-  finish(describe2, a.dseg, [&](int item, uint32_t st) {
-    int jv, h0, nr;
-    item2(item, jv, h0, nr);
-    const uint32_t r0 = st + (static_cast<uint32_t>(down_src(jv, h0)) & 15u) + wo;
-    const uint32_t rb = static_cast<uint32_t>(a.rbf);
-    const uint32_t wrow[4] = {r0, r0 + rb, r0 + 2u * rb, r0 + 3u * rb};
-    float acc[4];
-    dot_rows(wrow, nr, F, xs_s + static_cast<uint32_t>(jv * xrow_f), acc);
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float d = warp_sum(acc[r]);
-      if (lane == 0 && r < nr) part[(h0 + r) * kMaxK + jv] = d;
+  for (int it = 0; it < n2 && ok; ++it) {
+    if (!wait_slot()) {
+      ok = false;
+      break;
     }
-  });
+    const int nr = min(4, nh - 4 * qd_c);
+    const uint32_t r0 = wring_s + static_cast<uint32_t>(wslot * a.stage_bytes) +
+                        (static_cast<uint32_t>(down_src(jd_c, qd_c)) & 15u);
+    const uint32_t rb = static_cast<uint32_t>(a.rbf);
+    const uint32_t rows[4] = {r0, r0 + rb, r0 + 2u * rb, r0 + 3u * rb};
+    float acc[4];
+    dot_rows(acc, rows, F, xs_s + static_cast<uint32_t>(jd_c * xrow_f));
+    reduce_scatter<4>(acc, lane);  // row r's sum in lane 8 r
+    if ((lane & 7) == 0 && (lane >> 3) < nr) part[(4 * qd_c + (lane >> 3)) * kMaxK + jd_c] = acc[0];
+    release_slot();
+    adv2(jd_c, qd_c);
+    if (n2_iss < n2) {
+      issue2();
+      ++n2_iss;
+    }
+  }
   __syncthreads();
   for (int hl = threadIdx.x; hl < nh; hl += NW * 32) {
     float sum = 0.f;
@@ -1165,15 +1224,17 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
 // ------------------------------------------------------------------------------------------
 
 // Workspace layout.  A fixed header comes first, at offsets that do not depend on the shape
-// of a call: the one-token layer's grid-barrier counter (a 64-bit word that only grows) and
-// the router's tickets (one word per 16-token tile, room for every tile count the router
-// accepts).  Both must read zero in a fresh workspace and keep their meaning from call to
+// of a call: the one-token layer's grid-barrier counter and call counter (64-bit words that
+// only grow) and its tagged logits, then the router's tickets (one word per 16-token tile,
+// room for every tile count the router accepts).  Both must read zero in a fresh workspace and keep their meaning from call to
 // call, so one workspace sized for the largest shape serves every smaller one.  The scratch
 // regions (logits, dn rows, the grouped rows of the T > 16 path) follow the header and are
 // rewritten by every call.
 constexpr int kMaxRouterTiles = 65535;  // grid.y limit of the router launch
-constexpr size_t kWsBar = 0;
-constexpr size_t kWsTickets = 256;
+constexpr size_t kWsBar = 0;      // one-token layer: grid-barrier arrivals
+constexpr size_t kWsGen = 16;     // one-token layer: calls on this workspace
+constexpr size_t kWsXlog = 1024;  // one-token layer: tagged logits, up to 256 experts
+constexpr size_t kWsTickets = 4096;
 constexpr size_t kWsHeader = (kWsTickets + static_cast<size_t>(kMaxRouterTiles) * 4 + 255) & ~static_cast<size_t>(255);
 
 struct WsLayout {
@@ -1434,9 +1495,9 @@ qg_status one_token_layer(int type, const float *xn, const float *wr, const void
   a.wts_out = weights;
   a.act = act;
   a.x = x_inout;
-  const WsLayout L = ws_layout(1, k, E, H, F);
-  a.logits = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + L.logits);
   a.bar = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(ws) + kWsBar);
+  a.gen = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(ws) + kWsGen);
+  a.xlog = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(ws) + kWsXlog);
   a.rbh = static_cast<long long>(H / qk) * bb;
   a.rbf = static_cast<long long>(F / qk) * bb;
   switch (type) {

@@ -160,10 +160,11 @@ QG_API qg_status qgemm(int type, const void *w, const float *x, float *y, int64_
  * Pairs z = t*k + j index the per-pick buffers (act is f32 [T*k][F]).
  *
  * Workspace: moe_workspace_size(T, k, E, H, F) bytes of device memory, 16-byte aligned,
- * zero-filled by the caller once before its first use.  Its first 256.25 KB are a fixed
- * header whose words keep their meaning from call to call: the one-token layer's grid-barrier
- * counter (a 64-bit word that every moe_layer call at T = 1 advances) and the router's
- * per-tile tickets (every call leaves them at zero again).  Their offsets do not depend on the
+ * zero-filled by the caller once before its first use.  Its first 260 KB are a fixed header
+ * whose words keep their meaning from call to call: the one-token layer's grid-barrier
+ * counter and call counter (64-bit words that every moe_layer call at T = 1 advances), its
+ * logits tagged with the call, and the router's per-tile tickets (every call leaves them at
+ * zero again).  Their offsets do not depend on the
  * call's shape, so one workspace sized for the largest shape it will serve (the largest T, k,
  * E, H, F) may serve any call whose moe_workspace_size is not larger.  The rest holds scratch
  * that each call rewrites: the router logits, the per-pick down rows and, for more than 16

@@ -72,9 +72,10 @@ def test_moe_host_checks_need_no_gpu(lib):
     lib.moe_route_topk.argtypes = [P, P, I, I, I, I, P, P, P, P, SZ, P]
     lib.moe_expert_swiglu.argtypes = [I, P, P, I64, P, I, I, P, P, I, I, I, I, P, P, SZ, P]
     lib.moe_combine.argtypes = [I, P, I64, P, I, I, P, P, P, I, I, I, I, P, I, P, SZ, P]
-    # workspace: the fixed header (grid-barrier word, then one ticket word for each of up to
-    # 65535 router tiles), then router logits and dn rows, each rounded up to 256 bytes
-    header = (256 + 65535 * 4 + 255) // 256 * 256
+    # workspace: the fixed header (one-token grid-barrier and call counters, tagged logits,
+    # then one ticket word for each of up to 65535 router tiles), then router logits and dn
+    # rows, each rounded up to 256 bytes
+    header = (4096 + 65535 * 4 + 255) // 256 * 256
     n = lib.moe_workspace_size(8, 8, 128, 2048, 768)
     assert n == header + 8 * 128 * 4 + 8 * 8 * 2048 * 4
     # a workspace sized for a larger shape covers every smaller one
