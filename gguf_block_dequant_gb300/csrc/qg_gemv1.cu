@@ -61,7 +61,7 @@ QG_DEVICE void g1_status(unsigned int bits) { atomicOr(&g_qg_status_gemv, bits);
 // are used).  With GU the group loop is unrolled: every group's shared-memory offsets become
 // immediates of the loads.  One token takes the fused dot (Dec::dot1); several tokens decode
 // each weight once and multiply it into every token column.
-template <int QT, int NW, int CPS, int RR, int GU, int TT>
+template <int QT, int NW, int CPS, int RR, int GU, int TT, bool XREG = false>
 __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_constant__ CUtensorMap xmap, const G1Args a) {
   using D = Dec<QT>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -160,6 +160,15 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
   const int bfirst = D::block_first(lane);
 
   bool ok = mbar_wait(xfull, 0);
+  // XREG (one token, whole rows of GU groups): a lane multiplies the same activations in every
+  // row, so they are read from shared memory once and kept in registers
+  float4 xr[XREG ? GU : 1][D::NCH];
+  if constexpr (XREG) {
+#pragma unroll
+    for (int g = 0; g < GU; ++g)
+#pragma unroll
+      for (int ch = 0; ch < D::NCH; ++ch) xr[g][ch] = lds_f4(xs_s + static_cast<uint32_t>(g * (D::SG * 4)) + xo[ch]);
+  }
   float acc[RR];
   f2 acc2[RR][TT];
   int ci = 0, i = 0, cs = 0, done = 0;
@@ -194,7 +203,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
         if constexpr (TT == 1) {
           float4 xc[D::NCH];
 #pragma unroll
-          for (int ch = 0; ch < D::NCH; ++ch) xc[ch] = lds_f4(xg + xo[ch]);
+          for (int ch = 0; ch < D::NCH; ++ch) xc[ch] = XREG ? xr[XREG ? g : 0][ch] : lds_f4(xg + xo[ch]);
           const float aux = D::xaux(xc);
 #pragma unroll
           for (int r = 0; r < RR; ++r) u[r] = rp[r].load(goff, lane);
@@ -245,9 +254,10 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
     }
     if (++ci == my_c) {
       // row block done: the RR x TT sums (row r, token t at r * TT + t), reduce-scattered over
-      // the warp so that each lane owns one of them
+      // the warp so that each lane owns one of them (two when there are 64)
       constexpr int NV = RR * TT;
-      static_assert(NV <= 32, "one sum per lane");
+      constexpr int NH = NV == 64 ? 2 : 1;
+      static_assert(NV <= 64, "at most two sums per lane");
       float v[NV];
 #pragma unroll
       for (int r = 0; r < RR; ++r)
@@ -256,23 +266,30 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
       reduce_scatter<NV>(v, lane);
       const int i0 = rs_index<NV>(lane);
       const bool own = rs_owner<NV>(lane);
-      const int r0 = i0 / TT, t0 = i0 - r0 * TT;
       const uint32_t rb = rbA + static_cast<uint32_t>(rbl + i * lanes_rb);
       int j;
       uint32_t row;
       locate(rb, j, row);
       const uint32_t M = a.M[j];
       if (KW == 1) {
-        if (own && ok && t0 < a.T && row + r0 < M) a.y[j][static_cast<size_t>(t0) * M + row + r0] = v[0];
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const int r0 = (i0 + h) / TT, t0 = (i0 + h) - r0 * TT;
+          if (own && ok && t0 < a.T && row + r0 < M) a.y[j][static_cast<size_t>(t0) * M + row + r0] = v[h];
+        }
       } else {
         float *myred = red + warp * NV;
-        if (own) myred[i0] = v[0];
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+          if (own) myred[i0 + h] = v[h];
         named_bar_sync(1 + rbl, KW * 32);
-        if (kw == 0 && lane < NV) {
-          float s = 0.f;
-          for (int q = 0; q < KW; ++q) s += red[(rbl * KW + q) * NV + lane];
-          const int rr = lane / TT, tt = lane - rr * TT;
-          if (ok && tt < a.T && row + rr < M) a.y[j][static_cast<size_t>(tt) * M + row + rr] = s;
+        if (kw == 0) {
+          for (int idx = lane; idx < NV; idx += 32) {
+            float sum = 0.f;
+            for (int q = 0; q < KW; ++q) sum += red[(rbl * KW + q) * NV + idx];
+            const int rr = idx / TT, tt = idx - rr * TT;
+            if (ok && tt < a.T && row + rr < M) a.y[j][static_cast<size_t>(tt) * M + row + rr] = sum;
+          }
         }
         named_bar_sync(1 + rbl, KW * 32);  // red is reused by the next row block
       }
@@ -399,9 +416,9 @@ qg_status gemv1_plan(int nmat, const void *const *w, const float *x, float *cons
   return QG_OK;
 }
 
-template <int QT, int NW, int CPS, int RR, int GU, int TT>
+template <int QT, int NW, int CPS, int RR, int GU, int TT, bool XREG = false>
 qg_status gemv1_run(const G1Plan &P, cudaStream_t stream) {
-  auto kern = qgemv1_kernel<QT, NW, CPS, RR, GU, TT>;
+  auto kern = qgemv1_kernel<QT, NW, CPS, RR, GU, TT, XREG>;
   if (!set_smem_attr(reinterpret_cast<const void *>(kern), P.smem)) return QG_ECUDA;
   if (launch_pdl(kern, dim3(P.grid), dim3(NW * 32), P.smem, stream, P.map, P.a) != cudaSuccess) return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
@@ -409,13 +426,21 @@ qg_status gemv1_run(const G1Plan &P, cudaStream_t stream) {
 
 // One CTA shape, its group loop unrolled for the chunk sizes of the common row lengths
 // (2560 -> 5 groups, 4096 and 9728 -> chunks of 4, 1024 -> 2), a runtime loop otherwise.
-template <int QT, int NW, int CPS, int RR, int TT>
+template <int QT, int NW, int CPS, int RR, int TT, bool XREG = false>
 qg_status gemv1_cfg(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
                     int T, cudaStream_t stream) {
   G1Plan P;
   const qg_status r = gemv1_plan<QT, NW, CPS, RR, TT>(nmat, w, x, y, Ms, N, T, stream, P);
   if (r != QG_OK) return r;
-  if constexpr (TT == 1) {
+  if constexpr (TT == 1 && XREG) {
+    if (P.a.nchunks != 1) return QG_EUNSUPPORTED;
+    switch (P.a.gpc) {
+      case 5: return gemv1_run<QT, NW, CPS, RR, 5, TT, true>(P, stream);
+      case 4: return gemv1_run<QT, NW, CPS, RR, 4, TT, true>(P, stream);
+      case 2: return gemv1_run<QT, NW, CPS, RR, 2, TT, true>(P, stream);
+      default: return QG_EUNSUPPORTED;
+    }
+  } else if constexpr (TT == 1) {
     switch (P.a.gpc) {
       case 5: return gemv1_run<QT, NW, CPS, RR, 5, TT>(P, stream);
       case 4: return gemv1_run<QT, NW, CPS, RR, 4, TT>(P, stream);
@@ -427,11 +452,24 @@ qg_status gemv1_cfg(int nmat, const void *const *w, const float *x, float *const
 }
 
 // CTA shape per token count: two 8-warp CTAs per SM while the activations leave them room,
-// else one 8-warp CTA per SM (more shared memory and registers per warp).
+// else one 8-warp CTA per SM (more shared memory and registers per warp).  One token over a
+// very tall matrix (an output head) takes one 8-warp CTA per SM with 4-row blocks and the
+// activations in registers: every activation value then serves four rows and is read from
+// shared memory once per launch (151936 x 2560: 75 -> 71 us); the other shapes lose with it.
 template <int QT>
 qg_status gemv1_launch(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
                        int T, cudaStream_t stream) {
-  if (T == 1) return gemv1_cfg<QT, 8, 2, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
+  if (T == 1) {
+    if constexpr (Dec<QT>::QK == 32) {
+      long long rows = 0;
+      for (int j = 0; j < nmat; ++j) rows += Ms[j];
+      if (rows >= 65536) {
+        const qg_status r = gemv1_cfg<QT, 8, 1, 4, 1, true>(nmat, w, x, y, Ms, N, T, stream);
+        if (r != QG_EUNSUPPORTED) return r;
+      }
+    }
+    return gemv1_cfg<QT, 8, 2, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
+  }
   // several tokens: the 32-element types (the K-quants' lane state is too large to keep TT
   // accumulators beside it; they take the general kernel)
   if constexpr (QT != QG_TYPE_Q8_0 && QT != QG_TYPE_Q4_0) {
@@ -442,6 +480,7 @@ qg_status gemv1_launch(int nmat, const void *const *w, const float *x, float *co
     else if (T <= 4) r = gemv1_cfg<QT, 8, 2, 2, 4>(nmat, w, x, y, Ms, N, T, stream);
     if (r != QG_EUNSUPPORTED || T <= 2) return r;
     if (T <= 4) return gemv1_cfg<QT, 8, 1, 2, 4>(nmat, w, x, y, Ms, N, T, stream);
+    // 8 and 16 tokens: 2-row blocks (4-row blocks measured 15-20 % slower on the decode step)
     if (T <= 8) return gemv1_cfg<QT, 8, 1, 2, 8>(nmat, w, x, y, Ms, N, T, stream);
     return gemv1_cfg<QT, 8, 1, 2, 16>(nmat, w, x, y, Ms, N, T, stream);
   }

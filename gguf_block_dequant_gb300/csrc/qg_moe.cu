@@ -821,10 +821,6 @@ QG_DEVICE void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-QG_DEVICE void prefetch_l2(uintptr_t p, uint32_t n) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(n) : "memory");
-}
-
 // Grid-wide barrier for a cooperative grid: `bar` counts arrivals and only ever grows.  Every
 // launch adds exactly G per barrier and launches in a stream do not overlap this part (it comes
 // after the wait on the predecessor), so the arrivals of one barrier all return values in
@@ -889,6 +885,9 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
   // the workspace plus one (CTA 0 advances the count once every CTA is past the grid barrier,
   // so every CTA of a call reads the same count).
   pdl_wait();
+  // the token's activations into shared memory (128-byte swizzled rows) while the logits are
+  // computed and exchanged
+  copy_x_row(xs, 0, 0, a.xn, H, threadIdx.x, NW * 32);
   if (threadIdx.x == 0) s_misc[2] = static_cast<unsigned int>(ld_relaxed_u64(a.gen)) + 1u;
   __syncthreads();
   const unsigned int tag = s_misc[2];
@@ -920,9 +919,6 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
     }
     __syncthreads();
   }
-  // the token's activations into shared memory (128-byte swizzled rows) while the logits arrive
-  copy_x_row(xs, 0, 0, a.xn, H, threadIdx.x, NW * 32);
-
   // ---- phase 1: picks, then the gate/up row pairs.  The k greedy picks of the logits (ties
   // to the lowest expert id) are the experts of rank < k, rank(e) = #{e' : l[e'] > l[e] or
   // l[e'] == l[e] and e' < e}; the weights follow in pick order as in topk_token.
@@ -1010,21 +1006,10 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
       if (s_slot[j] < 0)
         for (int i = threadIdx.x; i < F; i += NW * 32) a.act[static_cast<size_t>(j) * F + i] = 0.f;
 
-  // hidden rows of phase 2 for this CTA, and their down rows into L2 now
+  // hidden rows of phase 2 for this CTA (their down rows are requested right after each
+  // warp's gate/up items, into the ring slots the gate/up phase leaves free)
   const int hA = static_cast<int>(static_cast<long long>(blockIdx.x) * H / G);
   const int hB = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * H / G);
-  if (warp == NW - 1) {
-    for (int u = lane; u < kv * (hB - hA); u += 32) {
-      const int jv = u / (hB - hA), h = hA + u % (hB - hA);
-      const uintptr_t p = reinterpret_cast<uintptr_t>(a.wd) +
-                          static_cast<uintptr_t>(s_slot[s_vz[jv]]) * static_cast<uintptr_t>(a.stride) +
-                          static_cast<uintptr_t>(h) * static_cast<uintptr_t>(a.rbf);
-      const uintptr_t al = p & ~static_cast<uintptr_t>(15);
-      const uintptr_t want = (p + static_cast<uintptr_t>(a.rbf) + 15) & ~static_cast<uintptr_t>(15);
-      const uintptr_t end = want < a.mend_d ? want : a.mend_d;
-      if (end > al) prefetch_l2(al, static_cast<uint32_t>(end - al));
-    }
-  }
 
   const uint32_t wo = static_cast<uint32_t>(D::woff(lane));
   uint32_t xo[D::NCH];

@@ -260,3 +260,18 @@ def test_static_weights_chain_matches_default(qg, oracle_lib, T):
         ref, bnd = oracle_lib.gemv(gs.Q8_0, ws[i], dims[i + 1], dims[i], xin, threads=4)
         assert_within_bound(b, ref, bnd, what=f"chain link {i} T={T}")
         xin = b
+
+
+@pytest.mark.parametrize("qtype,N", [(gs.Q8_0, 1024), (gs.Q8_0, 2560), (gs.Q4_0, 2048)])
+def test_tall_matrix_one_token(qg, oracle_lib, qtype, N):
+    """One token over more than 65536 rows takes the tall-matrix shape (4-row blocks, the
+    activations held in registers); a row count that leaves a partial last block, sampled rows
+    against the oracle, plus every row of the last blocks."""
+    M = 65536 + 7
+    w = gs.quant_blocks(qtype, M, N, seed=11, stream=qtype)
+    x = gs.activations(1, N, seed=11)
+    y = _run(qg, qtype, w, x, M, N)
+    rows = np.unique(np.concatenate([_sample_rows(M, n=200, seed=3), np.arange(M - 12, M)]))
+    rb = gs.row_bytes(qtype, N)
+    ref, bnd = oracle_lib.gemv(qtype, w.reshape(M, rb)[rows], len(rows), N, x, threads=4)
+    assert_within_bound(y[:, rows], ref, bnd, what=f"tall type {qtype} N={N}")
