@@ -468,7 +468,11 @@ qg_status gemv1_launch(int nmat, const void *const *w, const float *x, float *co
         if (r != QG_EUNSUPPORTED) return r;
       }
     }
-    return gemv1_cfg<QT, 8, 2, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
+    const qg_status r = gemv1_cfg<QT, 8, 2, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
+    if (r != QG_EUNSUPPORTED) return r;
+    // long rows whose activations leave half an SM too small a ring: one 16-warp CTA per SM
+    // holds them once beside a full ring
+    return gemv1_cfg<QT, 16, 1, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
   }
   // several tokens: the 32-element types (the K-quants' lane state is too large to keep TT
   // accumulators beside it; they take the general kernel)
