@@ -94,14 +94,27 @@ QG_DEVICE bool mbar_wait(uint64_t *bar, uint32_t parity) {
 // ---------------------------------------------------------------------------------------
 // Bulk copies global -> shared (the TMA engine's non-tensor form).  Both addresses must be
 // 16-byte aligned and the size a multiple of 16; completion is signalled on `bar` as
-// transaction bytes.
+// transaction bytes.  ONCE: the bytes are read once per launch (a weight stream), so their
+// L2 lines are the first to be evicted and the activations and outputs that the neighbouring
+// launches read stay resident.
 // ---------------------------------------------------------------------------------------
+template <bool ONCE = false>
 QG_DEVICE void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst_smem)),
-      "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
+  if constexpr (ONCE) {
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], pol;\n\t}" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+  } else {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+  }
 }
 
 // 16-byte asynchronous global -> shared copy (both addresses 16-byte aligned); completes at

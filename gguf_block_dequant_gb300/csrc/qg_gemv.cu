@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(NW * 32, (TT == 1 && NW == 8) ? 2 : 1) qgemv_k
       src = wbase + static_cast<uintptr_t>((rb * RR + lane) * a.row_bytes + u.c * chunk_bytes);
       dst = st + lane * a.seg_slot;
     }
-    warp_bulk_copies(dst, src, n, b.mend, &wbar[warp * kMaxNS + s], lane);
+    warp_bulk_copies<true>(dst, src, n, b.mend, &wbar[warp * kMaxNS + s], lane);
   };
 
   // Prologue: the first NS - 1 items.  Normally issued after the wait on the preceding kernel

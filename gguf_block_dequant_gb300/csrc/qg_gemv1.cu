@@ -5,12 +5,15 @@
 // y[m] = sum_k W[m][k] * x[k]  (matmulQ8 / matmulQ4 / the Q4_K row dot of WG_GEMM_Q4K on the
 // engine pages), raw GGUF blocks decoded in registers, f32 accumulation.
 //
-// Same work mapping as the general kernel (qg_gemv.cu): persistent CTAs with a balanced
-// contiguous range of RR-row blocks each; every warp streams its own row blocks through a
-// private ring of shared-memory slots with bulk copies and decodes them with the lane decoders
-// of qg_decode.cuh (two lanes per block, sixteen blocks per 512-element group); when a CTA
-// has fewer row blocks than warps, KW warps split each row block's K chunks and meet at a
-// named barrier.  What is specialised away, because it cost instruction issue in every stage:
+// Work mapping: persistent CTAs with a balanced contiguous range of RR-row blocks each; a row
+// block is cut into K chunks when its rows do not fit a stage (or to give every warp work), and
+// the CTA's (row block, chunk) items are dealt to its warps in contiguous ranges equal to
+// within one item, so that no warp streams more than its share when the CTA's row blocks do
+// not divide among its warps.  Every warp streams its items through a private ring of
+// shared-memory slots with bulk copies and decodes them with the lane decoders of
+// qg_decode.cuh (two lanes per block, sixteen blocks per 512-element group); a row block whose
+// chunks span two warps' ranges is summed from their parts in shared memory, in chunk order.
+// What is specialised away, because it cost instruction issue in every stage:
 //   - 32-bit row and byte offsets (every matrix < 4 GiB), matrix bounds precomputed;
 //   - a stage of whole rows is one copy issued by lane 0 alone (rows are contiguous);
 //   - no tail handling of unaligned rows (rows start 16-byte aligned by construction);
@@ -45,7 +48,6 @@ struct G1Args {
   uint32_t seg;          // slot bytes per row of a chunked stage
   uint32_t stage_bytes;  // bytes per slot
   int NS;
-  int max_kw;
   int N;
   int T;                 // token columns (<= TT of the kernel)
   uint32_t xtok;         // shared-memory bytes of one token's activations
@@ -68,7 +70,7 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *wbar = reinterpret_cast<uint64_t *>(smem);  // [NW][kNS]
   uint64_t *xfull = wbar + NW * kNS;
-  float *red = reinterpret_cast<float *>(smem + a.off_red);  // [NW][RR * TT] (K-split partial sums)
+  float *red = reinterpret_cast<float *>(smem + a.off_red);  // [2 NW][RR * TT] parts of split row blocks
   uint8_t *xs = smem + a.off_x;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -76,14 +78,17 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
   const uint32_t rbA = static_cast<uint32_t>(static_cast<unsigned long long>(blockIdx.x) * a.rblocks / G);
   const uint32_t rbB = static_cast<uint32_t>(static_cast<unsigned long long>(blockIdx.x + 1) * a.rblocks / G);
   const int nrb = static_cast<int>(rbB - rbA);
-  int KW = 1;
-  if (nrb < NW) KW = max(1, min(NW / max(nrb, 1), a.max_kw));
-  const int kw = warp % KW, rbl = warp / KW;
-  const int lanes_rb = NW / KW;  // row-block lanes of the CTA
-  const int my_n = (rbl < lanes_rb && rbl < nrb) ? (nrb - rbl + lanes_rb - 1) / lanes_rb : 0;
   const int nc = a.nchunks;
-  const int my_c = (nc - kw + KW - 1) / KW;  // chunks kw, kw + KW, ... of each row block
-  const int items = my_n * my_c;
+  // The CTA's items are its (row block, chunk) pairs in row-block-major order.  Whole rows
+  // (nc == 1): warp w takes row blocks w, w + NW, ... (the CTA streams neighbouring blocks at
+  // any time).  Chunked rows: the first NWa warps take contiguous ranges of items, equal to
+  // within one item, every range non-empty.
+  const int n_items = nrb * nc;
+  const int NWa = max(1, min(NW, n_items));
+  auto kb = [&](int w) { return w * n_items / NWa; };
+  const int k0 = nc == 1 ? warp : (warp < NWa ? kb(warp) : 0);
+  const int items = nc == 1 ? (warp < n_items ? (n_items - warp + NW - 1) / NW : 0) : (warp < NWa ? kb(warp + 1) - k0 : 0);
+  const int istep = nc == 1 ? NW : 1;  // row blocks from one whole-row item to the next
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NW * kNS; ++i) mbar_init(&wbar[i], 1);
@@ -105,9 +110,9 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
     row = (rb - a.rb0[j]) * RR;
   };
 
-  // issue item (i, ci) -- the i-th row block of this warp, its ci-th chunk -- into slot s
-  auto issue = [&](int i, int ci, int s) {
-    const uint32_t rb = rbA + static_cast<uint32_t>(rbl + i * lanes_rb);
+  // issue chunk c of the CTA's row block i into slot s
+  auto issue = [&](int i, int c, int s) {
+    const uint32_t rb = rbA + static_cast<uint32_t>(i);
     int j;
     uint32_t row;
     locate(rb, j, row);
@@ -117,40 +122,41 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
       if (lane == 0) {
         const uint32_t bytes = nr * a.row_bytes;
         mbar_arrive_expect_tx(&mybar[s], bytes);
-        bulk_g2s(ring + s * a.stage_bytes, src, bytes, &mybar[s]);
+        bulk_g2s<true>(ring + s * a.stage_bytes, src, bytes, &mybar[s]);
       }
     } else {
-      const int c = kw + ci * KW;
       const uint32_t cb = (c == nc - 1) ? a.row_bytes - static_cast<uint32_t>(c) * a.chunk_bytes : a.chunk_bytes;
       if (lane == 0) mbar_arrive_expect_tx(&mybar[s], nr * cb);
       __syncwarp();
       if (static_cast<uint32_t>(lane) < nr)
-        bulk_g2s(ring + s * a.stage_bytes + lane * a.seg, src + lane * a.row_bytes + static_cast<uint32_t>(c) * a.chunk_bytes,
+        bulk_g2s<true>(ring + s * a.stage_bytes + lane * a.seg, src + lane * a.row_bytes + static_cast<uint32_t>(c) * a.chunk_bytes,
                  cb, &mybar[s]);
     }
   };
 
-  // prologue: the first NS - 1 items (before the wait on the predecessor with static weights)
-  int ii = 0, ic = 0, is = 0, issued = 0;
+  // prologue: the first NS - 1 items.  With static weights the first item of every warp is
+  // requested before the wait on the predecessor and the rest after the activations' copy
+  // (more weight requests in flight at the wait only delay the activations).
+  int ii = k0 / nc, ic = k0 - (k0 / nc) * nc, is = 0, issued = 0;
   auto advance_issue = [&]() {
-    if (++ic == my_c) {
+    if (++ic == nc) {
       ic = 0;
-      ++ii;
+      ii += istep;
     }
     is = (is + 1 == a.NS) ? 0 : is + 1;
     ++issued;
   };
-  auto prologue = [&]() {
-    for (int k = 0; k < a.NS - 1 && issued < items; ++k) {
+  auto prologue = [&](int upto) {
+    while (issued < upto && issued < items) {
       issue(ii, ic, is);
       advance_issue();
     }
   };
-  if (a.early_weights) prologue();
+  if (a.early_weights) prologue(1);
   pdl_wait();
   pdl_launch_dependents();
   if (threadIdx.x == 0) load_x(xs, &xmap, a.T, a.N, 0, a.xR, a.box_rows, xfull);
-  if (!a.early_weights) prologue();
+  prologue(a.NS - 1);
 
   const uint32_t wo = static_cast<uint32_t>(D::woff(lane));
   const uint32_t xs_s = smem_u32(xs);
@@ -169,17 +175,19 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
 #pragma unroll
       for (int ch = 0; ch < D::NCH; ++ch) xr[g][ch] = lds_f4(xs_s + static_cast<uint32_t>(g * (D::SG * 4)) + xo[ch]);
   }
+  constexpr int NV = RR * TT;
   float acc[RR];
   f2 acc2[RR][TT];
-  int ci = 0, i = 0, cs = 0, done = 0;
+  int i = k0 / nc, c = k0 - (k0 / nc) * nc, cs = 0, done = 0;  // the compute cursor
+  int c_first = c;  // first chunk of the current segment (the items of one row block in a row)
   uint32_t phase = 0;
-  for (int t = 0; t < items; ++t) {
+  for (int it = 0; it < items; ++it) {
     if (ok && issued < items) {
       issue(ii, ic, is);
       advance_issue();
     }
-    const int c = kw + ci * KW;
-    if (ci == 0) {
+    if (c == 0 || it == 0) {
+      c_first = c;
 #pragma unroll
       for (int r = 0; r < RR; ++r) {
         acc[r] = 0.f;
@@ -238,7 +246,16 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
 #pragma unroll
         for (int g = 0; g < GU; ++g)
           if (g < gl) group(g);
-        if (c == nc - 1 && !a.last_full && gl * D::SG + bfirst < a.N - c * a.gpc * D::SG) group(gl);
+        if (c == nc - 1 && !a.last_full && gl * D::SG + bfirst < a.N - c * a.gpc * D::SG) {
+          if constexpr (XREG) {
+            // xr is indexed by constants only, or it would live in local memory
+#pragma unroll
+            for (int g = 0; g < GU; ++g)
+              if (g == gl) group(g);
+          } else {
+            group(gl);
+          }
+        }
       } else if (c < nc - 1) {
         for (int g = 0; g < a.gpc; ++g) group(g);
       } else {
@@ -252,10 +269,12 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
       cs = 0;
       phase ^= 1u;
     }
-    if (++ci == my_c) {
-      // row block done: the RR x TT sums (row r, token t at r * TT + t), reduce-scattered over
-      // the warp so that each lane owns one of them (two when there are 64)
-      constexpr int NV = RR * TT;
+    if (c == nc - 1 || it == items - 1) {
+      // end of a segment (this warp's items of row block i): the RR x TT sums (row r, token t
+      // at r * TT + t), reduce-scattered over the warp so that each lane owns one of them (two
+      // when there are 64).  A whole row block goes to y; a part of one split between warps
+      // goes to its slot of red: the part that starts at chunk 0 to slot 2 (w + 1), w its
+      // warp, the part that starts at a later chunk (at its warp's first item) to slot 2 w + 1.
       constexpr int NH = NV == 64 ? 2 : 1;
       static_assert(NV <= 64, "at most two sums per lane");
       float v[NV];
@@ -266,35 +285,47 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
       reduce_scatter<NV>(v, lane);
       const int i0 = rs_index<NV>(lane);
       const bool own = rs_owner<NV>(lane);
-      const uint32_t rb = rbA + static_cast<uint32_t>(rbl + i * lanes_rb);
-      int j;
-      uint32_t row;
-      locate(rb, j, row);
-      const uint32_t M = a.M[j];
-      if (KW == 1) {
+      if (c_first == 0 && c == nc - 1) {
+        int j;
+        uint32_t row;
+        locate(rbA + static_cast<uint32_t>(i), j, row);
+        const uint32_t M = a.M[j];
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
           const int r0 = (i0 + h) / TT, t0 = (i0 + h) - r0 * TT;
           if (own && ok && t0 < a.T && row + r0 < M) a.y[j][static_cast<size_t>(t0) * M + row + r0] = v[h];
         }
       } else {
-        float *myred = red + warp * NV;
+        float *slot = red + (c_first == 0 ? 2 * (warp + 1) : 2 * warp + 1) * NV;
 #pragma unroll
         for (int h = 0; h < NH; ++h)
-          if (own) myred[i0 + h] = v[h];
-        named_bar_sync(1 + rbl, KW * 32);
-        if (kw == 0) {
-          for (int idx = lane; idx < NV; idx += 32) {
-            float sum = 0.f;
-            for (int q = 0; q < KW; ++q) sum += red[(rbl * KW + q) * NV + idx];
-            const int rr = idx / TT, tt = idx - rr * TT;
-            if (ok && tt < a.T && row + rr < M) a.y[j][static_cast<size_t>(tt) * M + row + rr] = sum;
-          }
-        }
-        named_bar_sync(1 + rbl, KW * 32);  // red is reused by the next row block
+          if (own) slot[i0 + h] = v[h];
       }
-      ci = 0;
-      ++i;
+    }
+    if (++c == nc) {
+      c = 0;
+      i += istep;
+    }
+  }
+  if (nc > 1) {
+    // row blocks split between warps: warp w, the first boundary inside such a block, sums its
+    // parts in chunk order (deterministic) and writes y
+    __syncthreads();
+    if (warp >= 1 && warp < NWa) {
+      const int b = kb(warp);
+      const int rbl = b / nc, lo = rbl * nc;
+      if (b != lo && kb(warp - 1) <= lo) {
+        int j;
+        uint32_t row;
+        locate(rbA + static_cast<uint32_t>(rbl), j, row);
+        const uint32_t M = a.M[j];
+        for (int idx = lane; idx < NV; idx += 32) {
+          float sum = red[2 * warp * NV + idx];
+          for (int w = warp; w < NWa && kb(w) < lo + nc; ++w) sum += red[(2 * w + 1) * NV + idx];
+          const int rr = idx / TT, tt = idx - rr * TT;
+          if (ok && tt < a.T && row + rr < M) a.y[j][static_cast<size_t>(tt) * M + row + rr] = sum;
+        }
+      }
     }
   }
   if (!ok) {
@@ -331,7 +362,7 @@ qg_status gemv1_plan(int nmat, const void *const *w, const float *x, float *cons
   const long long xres = ((static_cast<long long>(T) * xtok + 1023) / 1024) * 1024;
   const long long budget = (CPS == 1 ? dev.smem_optin : dev.smem_per_sm / CPS) - 4096;
   const uint32_t hdr = 1024;
-  const uint32_t red_bytes = NW * RR * TT * 4;
+  const uint32_t red_bytes = 2 * NW * RR * TT * 4;  // two part slots per warp
   G1Args a{};
   unsigned long long rblocks = 0;
   for (int j = 0; j < nmat; ++j) {
@@ -370,9 +401,10 @@ qg_status gemv1_plan(int nmat, const void *const *w, const float *x, float *cons
     seg = static_cast<long long>(gpc) * D::GB;
     stage = RR * seg;
   }
-  // when the CTAs have fewer row blocks than warps, the warps split K: give them chunks
+  // when the CTAs have fewer row blocks than warps, cut the rows into chunks so that every
+  // warp gets items
   if (rb_per_cta < NW) {
-    const int want_kw = static_cast<int>(std::min<long long>(NW, NW / std::max<long long>(1, rb_per_cta)));
+    const int want_kw = static_cast<int>(std::min<long long>(NW, (NW + rb_per_cta - 1) / std::max<long long>(1, rb_per_cta)));
     const int floor_g = std::min(ngroups, (2048 + D::GB - 1) / D::GB);
     while (gpc > floor_g && (ngroups + gpc - 1) / gpc < want_kw) {
       int g2 = std::max(floor_g, gpc / 2);
@@ -398,7 +430,6 @@ qg_status gemv1_plan(int nmat, const void *const *w, const float *x, float *cons
   a.seg = static_cast<uint32_t>(seg);
   a.stage_bytes = static_cast<uint32_t>(stage);
   a.NS = NS;
-  a.max_kw = nchunks;
   a.N = static_cast<int>(N);
   a.T = T;
   a.xtok = static_cast<uint32_t>(xtok);
@@ -460,9 +491,9 @@ template <int QT>
 qg_status gemv1_launch(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
                        int T, cudaStream_t stream) {
   if (T == 1) {
+    long long rows = 0;
+    for (int j = 0; j < nmat; ++j) rows += Ms[j];
     if constexpr (Dec<QT>::QK == 32) {
-      long long rows = 0;
-      for (int j = 0; j < nmat; ++j) rows += Ms[j];
       if (rows >= 65536) {
         const qg_status r = gemv1_cfg<QT, 8, 1, 4, 1, true>(nmat, w, x, y, Ms, N, T, stream);
         if (r != QG_EUNSUPPORTED) return r;

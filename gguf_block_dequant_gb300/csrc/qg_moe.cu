@@ -1100,7 +1100,7 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
         n = static_cast<uint32_t>(a.rbh);
         mend = lane ? a.mend_u : a.mend_g;
       }
-      warp_bulk_copies(wring + islot * a.stage_bytes + lane * a.gseg, src, n, mend, &wbar[warp * kMaxNS + islot], lane);
+      warp_bulk_copies<true>(wring + islot * a.stage_bytes + lane * a.gseg, src, n, mend, &wbar[warp * kMaxNS + islot], lane);
       next_slot();
       adv(jvi, ii);
     };
@@ -1153,7 +1153,7 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
       src = down_src(jd_i, qd_i);
       n = static_cast<uint32_t>(min(4, nh - 4 * qd_i)) * static_cast<uint32_t>(a.rbf);
     }
-    warp_bulk_copies(wring + islot * a.stage_bytes, src, n, a.mend_d, &wbar[warp * kMaxNS + islot], lane);
+    warp_bulk_copies<true>(wring + islot * a.stage_bytes, src, n, a.mend_d, &wbar[warp * kMaxNS + islot], lane);
     next_slot();
     adv2(jd_i, qd_i);
   };

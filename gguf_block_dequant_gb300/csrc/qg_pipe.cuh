@@ -49,6 +49,8 @@ QG_DEVICE uint32_t stage_copy(uint8_t *dst, uintptr_t src, uint32_t n, uintptr_t
 
 // One bulk copy per active lane (each lane's own segment), all on one mbarrier: the byte
 // count of every segment is added to the barrier's transaction count before any copy starts.
+// ONCE as for bulk_g2s.
+template <bool ONCE = false>
 QG_DEVICE void warp_bulk_copies(uint8_t *dst, uintptr_t src, uint32_t n, uintptr_t mend, uint64_t *bar, int lane) {
   uint32_t nb = 0;
   if (n) nb = stage_copy(dst, src, n, mend);
@@ -57,7 +59,7 @@ QG_DEVICE void warp_bulk_copies(uint8_t *dst, uintptr_t src, uint32_t n, uintptr
   __syncwarp();
   if (nb) {
     fence_proxy_async_smem();  // the slot's previous bytes were read through the generic proxy
-    bulk_g2s(dst, reinterpret_cast<const void *>(src & ~static_cast<uintptr_t>(15)), nb, bar);
+    bulk_g2s<ONCE>(dst, reinterpret_cast<const void *>(src & ~static_cast<uintptr_t>(15)), nb, bar);
   }
 }
 

@@ -186,6 +186,21 @@ def test_kquant_full_size(qg, oracle_lib, qtype, M, N, T):
     assert_within_bound(y[:, rows], ref, bnd, what=f"type {qtype} {M}x{N} T={T}")
 
 
+@pytest.mark.parametrize("qtype,M,N,T", [(gs.Q8_0, 2560, 9728, 1), (gs.Q8_0, 2560, 4096, 1), (gs.Q8_0, 2561, 9728, 4),
+                                          (gs.Q8_0, 2560, 9728, 16), (gs.Q4_0, 999, 9728, 8), (gs.Q4_K, 640, 17408, 1),
+                                          (gs.Q6_K, 333, 17408, 1), (gs.Q8_0, 31, 9728, 1)])
+def test_row_blocks_split_between_warps(qg, oracle_lib, qtype, M, N, T):
+    """Few row blocks per CTA and rows cut into K chunks: the CTA's (row block, chunk) items are
+    dealt to its warps in contiguous ranges, so many row blocks are summed from the parts of
+    two or more warps (and with 31 rows some CTAs have fewer items than warps).  Every row
+    against the oracle."""
+    w = gs.quant_blocks(qtype, M, N, seed=5, stream=300 + qtype)
+    x = gs.activations(T, N, seed=5)
+    y = _run(qg, qtype, w, x, M, N)
+    ref, bnd = oracle_lib.gemv(qtype, w, M, N, x, threads=8)
+    assert_within_bound(y, ref, bnd, what=f"split type {qtype} {M}x{N} T={T}")
+
+
 def test_config1_full(qg, oracle_lib):
     """Q8_0 1024 x 1024, T = 1, seed 0: every row against the oracle."""
     M = N = 1024
@@ -262,11 +277,12 @@ def test_static_weights_chain_matches_default(qg, oracle_lib, T):
         xin = b
 
 
-@pytest.mark.parametrize("qtype,N", [(gs.Q8_0, 1024), (gs.Q8_0, 2560), (gs.Q4_0, 2048)])
+@pytest.mark.parametrize("qtype,N", [(gs.Q8_0, 1024), (gs.Q8_0, 2560), (gs.Q8_0, 2304), (gs.Q4_0, 2048), (gs.Q4_0, 1792)])
 def test_tall_matrix_one_token(qg, oracle_lib, qtype, N):
     """One token over more than 65536 rows takes the tall-matrix shape (4-row blocks, the
     activations held in registers); a row count that leaves a partial last block, sampled rows
-    against the oracle, plus every row of the last blocks."""
+    against the oracle, plus every row of the last blocks.  2304 and 1792 end in a partial
+    512-element group (4.5 and 3.5 groups per row)."""
     M = 65536 + 7
     w = gs.quant_blocks(qtype, M, N, seed=11, stream=qtype)
     x = gs.activations(1, N, seed=11)
