@@ -499,7 +499,7 @@ def run_ours(args):
 
 
 def run_detail(torch, qg, D, stream, args, hbm):
-    """Secondary numbers: T = 4 / 16 steps, per-projection T = 1 times, K-quant shapes, MoE."""
+    """Secondary numbers: T = 4 / 8 / 16 steps, per-projection T = 1 times, K-quant shapes, MoE."""
     out = {}
     wbytes = step_weight_bytes(args.layers)
     other = "ordered" if args.weights == "static" else "static"
@@ -512,7 +512,7 @@ def run_detail(torch, qg, D, stream, args, hbm):
     out[f"decode_step_T{args.tokens}_{other}_weights"] = {"GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
                                                          "us_per_step": round(el / steps * 1e6, 1)}
     del g
-    for T in (4, 16):
+    for T in (4, 8, 16):
         if T == args.tokens:
             continue
         g = capture(torch, lambda T=T: D.step(T), stream)

@@ -544,8 +544,27 @@ qg_status launch_cfg(int nmat, const void *const *w, const float *x, float *cons
 template <int QT, int TT>
 qg_status launch_t(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
                    int T, cudaStream_t stream) {
+  // several tokens: rows across lanes (qg_gemv_mt.cu) when the launch has at least two
+  // 16-row groups per SM; with fewer, a CTA's single group leaves its warps short of work and
+  // the lean kernel's 2-row blocks win (2560 x 4096 at T = 4: 7.9 vs 9.2 us)
+  long long groups = 0;
+  for (int j = 0; j < nmat; ++j) groups += (Ms[j] + 15) / 16;
+  const bool mt_first = TT > 1 && groups >= 2LL * qg::device_info().sms;
+  if constexpr (TT > 1) {
+    if (mt_first) {
+      const qg_status r0 = qg::gemv_mt_launch<QT>(nmat, w, x, y, Ms, N, T, stream);
+      if (r0 != QG_EUNSUPPORTED) return r0;
+    }
+  }
   const qg_status r = qg::gemv1_launch<QT>(nmat, w, x, y, Ms, N, T, stream);
   if (r != QG_EUNSUPPORTED) return r;
+  if constexpr (TT > 1) {
+    // activations too long to stay resident in one CTA: K split over a cluster
+    if (!mt_first) {
+      const qg_status r2 = qg::gemv_mt_launch<QT>(nmat, w, x, y, Ms, N, T, stream);
+      if (r2 != QG_EUNSUPPORTED) return r2;
+    }
+  }
   if constexpr (TT == 1) {
     if constexpr (QT == QG_TYPE_Q4_K) {
       using D = Dec<QT>;

@@ -73,6 +73,12 @@ template <int QT>
 qg_status gemv1_launch(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
                        int T, cudaStream_t stream);
 
+// GEMV over 2..16 token columns, Q8_0 / Q4_0 rows of whole 256-element units, rows across
+// lanes (qg_gemv_mt.cu); QG_EUNSUPPORTED with nothing launched for other shapes
+template <int QT>
+qg_status gemv_mt_launch(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms,
+                         int64_t N, int T, cudaStream_t stream);
+
 qg_status gemv_multi_dispatch(int type, int n, const void *const *w, const float *x, float *const *y,
                               const int64_t *M, int64_t N, int T, cudaStream_t s);
 unsigned int read_status_gemv(bool clear);

@@ -92,6 +92,22 @@ inline bool encode_x_map(CUtensorMap *map, const float *x, long long rows, long 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map over a token-major f32 [T][K] activation matrix seen as K/32 rows of tt token
+// slots of 32 floats: a box (32 floats, tt tokens, box_rows rows) lands as [row][token][32]
+// (row r, token t at 32-float row r * tt + t of the box), with the 128-byte swizzle; token
+// slots >= T read as zero.  K % 32 == 0, tt <= 256, box_rows <= 256.
+inline bool encode_x_map_tok(CUtensorMap *map, const float *x, long long T, long long K, int tt, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t gdim[3] = {32, static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(K / 32)};
+  const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(K) * 4u, 128};
+  const cuuint32_t boxd[3] = {32, static_cast<cuuint32_t>(tt), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(x), gdim, gstride, boxd, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Largest box height (multiple of 8, <= 256) dividing rows.
 inline int box_rows_for(int rows) {
   int box = 8;
