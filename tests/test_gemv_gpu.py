@@ -114,6 +114,26 @@ def test_gemv_one_hot_edge_blocks(qg, oracle_lib, qtype, T, aligned):
             assert np.array_equal(y[t], W[:, k]), (qtype, T, k, np.nonzero(y[t] != W[:, k])[0][:4])
 
 
+@pytest.mark.parametrize("qtype", [gs.Q8_0, gs.Q4_0])
+@pytest.mark.parametrize("M,N,T", [(4874, 1024, 4), (4874, 1024, 16), (26, 4096, 16)])
+def test_multi_token_edge_blocks_rows_across_lanes(qg, oracle_lib, qtype, M, N, T):
+    """The edge blocks through the rows-across-lanes decoders: 4874 rows are 305 16-row groups
+    (at least two per SM, so that kernel goes first, and the last group is partial); 26 rows of
+    4096 at T = 16 do not fit one CTA's shared memory with their activations, so K is split
+    over a cluster.  One-hot activations: every output is one dequantized weight, bit for bit."""
+    w = eb.matrix_with_edge_blocks(qtype, M, N, seed=13)
+    W = oracle_lib.dequant(qtype, w, M, N)
+    cols = list(range(3, N, 37)) + [0, N - 1]
+    for start in range(0, len(cols), T):
+        ks = cols[start:start + T]
+        x = np.zeros((len(ks), N), np.float32)
+        for t, k in enumerate(ks):
+            x[t, k] = 1.0
+        y = _run(qg, qtype, w, x, M, N)
+        for t, k in enumerate(ks):
+            assert np.array_equal(y[t], W[:, k]), (qtype, M, N, T, k, np.nonzero(y[t] != W[:, k])[0][:4])
+
+
 @pytest.mark.parametrize("qtype", TYPES)
 def test_gemv_zero_input_and_zero_rows(qg, qtype):
     M, N = 70, 1024
@@ -230,6 +250,27 @@ def test_gemv_multi_matches_separate_calls(qg, oracle_lib, qtype, T):
             continue
         ref, bnd = oracle_lib.gemv(qtype, ws[j], M, N, x, threads=4)
         assert_within_bound(yd[j].cpu().numpy(), ref, bnd, what=f"multi type {qtype} j={j} T={T}")
+
+
+@pytest.mark.parametrize("qtype", [gs.Q8_0, gs.Q4_0])
+@pytest.mark.parametrize("T", [5, 16])
+def test_gemv_multi_rows_across_lanes(qg, oracle_lib, qtype, T):
+    """qgemv_multi over 377 16-row groups (the rows-across-lanes kernel goes first), matrices
+    with partial last groups and one empty: every row of every matrix against the oracle."""
+    N = 2560
+    Ms = [4100, 0, 1000, 903]
+    x = gs.activations(T, N, seed=T, stream=72)
+    ws = [gs.quant_blocks(qtype, max(M, 1), N, seed=j, stream=90 + j) for j, M in enumerate(Ms)]
+    wd = [to_dev(w, torch) for w in ws]
+    yd = [torch.full((T, max(M, 1)), float("nan"), dtype=torch.float32, device="cuda")[:, :M].contiguous() for M in Ms]
+    qg.qgemv_multi(qtype, wd, yd, to_dev(x, torch), N, T)
+    torch.cuda.synchronize()
+    assert qg.device_status() == 0
+    for j, M in enumerate(Ms):
+        if M == 0:
+            continue
+        ref, bnd = oracle_lib.gemv(qtype, ws[j], M, N, x, threads=8)
+        assert_within_bound(yd[j].cpu().numpy(), ref, bnd, what=f"multi rows-across-lanes type {qtype} j={j} T={T}")
 
 
 def test_gemv_multi_rejects(qg):
