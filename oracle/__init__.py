@@ -63,6 +63,9 @@ def lib():
             L.og_moe_gate_up.argtypes = [I, P, P, I64, P, P, P, I64, I, I64, I64, P, P, P, P, P, I]
             L.og_moe_down_combine.argtypes = [I, P, I64, P, P, P, P, P, I64, I, I64, I64, I, P, P, P, P, I]
             L.og_max_threads.restype = I
+            L.og_embed_rows.argtypes = [I, P, I64, I64, P, I64, ctypes.c_float, P]
+            L.og_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double, P]
+            L.og_argmax_rows.argtypes = [P, I64, I64, P]
             _lib = L
     return _lib
 
@@ -186,3 +189,32 @@ def moe_layer(qtype, experts, gate_off, up_off, down_off, expert_stride, wr, xn,
                                           1, threads)
     return dict(logits=lg, bound_logits=blg, ids=ids, weights=wts, gate=g, up=u, act=act, bound_gate=bg,
                 bound_up=bu, dn=dn, bound_dn=bdn, out=out, bound_out=bout)
+
+
+def embed_rows(qtype: int, table: np.ndarray, V: int, N: int, ids, scale: float = 1.0) -> np.ndarray:
+    """out[i][k] = dequantized table[ids[i]][k] * scale (f64 product rounded once to f32)."""
+    b = _u8(table)
+    ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+    out = np.empty((ids.size, N), dtype=np.float32)
+    _check(lib().og_embed_rows(qtype, _p(b), V, N, _p(ids), ids.size, float(np.float32(scale)), _p(out)), "embed_rows")
+    return out
+
+
+def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    """y[t][k] = x[t][k] * w[k] / sqrt(mean_k x[t][k]^2 + eps), float64 [T][N]."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    x2 = x.reshape(-1, x.shape[-1])
+    w = np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
+    T, N = x2.shape
+    y = np.empty((T, N), dtype=np.float64)
+    _check(lib().og_rmsnorm(_p(x2), _p(w), T, N, float(eps), _p(y)), "rmsnorm")
+    return y
+
+
+def argmax_rows(v: np.ndarray) -> np.ndarray:
+    """Lowest index of each row's largest value (NaN never picked; an all-NaN row gives 0)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    v2 = v.reshape(-1, v.shape[-1])
+    ids = np.empty(v2.shape[0], dtype=np.int32)
+    _check(lib().og_argmax_rows(_p(v2), v2.shape[0], v2.shape[1], _p(ids)), "argmax_rows")
+    return ids

@@ -341,3 +341,56 @@ int og_moe_down_combine(int type, const uint8_t *w_down, int64_t expert_stride, 
     }
   return OG_OK;
 }
+
+/* Embedding row gather (embedQ8 in qwen3_moe_ssd.js, embedQ6K in gemma4_moe_ssd.js):
+ *   out[i][k] = w(ids[i], k) * scale,   k < N
+ * where w(r, k) is element k of row r of the [V][N] table, dequantized by og_block_value, and
+ * the product is taken in float64 and rounded once to f32 (embedQ6K multiplies by its
+ * p.scale; embedQ8 has none, scale = 1).  An id outside [0, V) is an error. */
+int og_embed_rows(int type, const uint8_t *table, int64_t V, int64_t N, const int32_t *ids, int64_t n,
+                  float scale, float *out) {
+  int qk, bb;
+  if (og_block_shape(type, &qk, &bb)) return OG_EBADTYPE;
+  if (N % qk || V < 0 || n < 0) return OG_EBADSHAPE;
+  int64_t nb = N / qk;
+  for (int64_t i = 0; i < n; ++i) {
+    if (ids[i] < 0 || ids[i] >= V) return OG_EBADSHAPE;
+    const uint8_t *row = table + (int64_t)ids[i] * nb * bb;
+    for (int64_t k = 0; k < N; ++k) {
+      double v = (double)og_block_value(type, row + (k / qk) * bb, (int)(k % qk));
+      out[i * N + k] = (float)(v * (double)scale);
+    }
+  }
+  return OG_OK;
+}
+
+/* RMSNorm (rmsnorm in qwen3_moe_ssd.js): per row t,
+ *   s_t = 1 / sqrt(mean_k x[t][k]^2 + eps),   y[t][k] = x[t][k] * s_t * w[k]
+ * in float64 (the page scales x first, then multiplies by w). */
+int og_rmsnorm(const float *x, const float *w, int64_t T, int64_t N, double eps, double *y) {
+  if (T < 0 || N <= 0) return OG_EBADSHAPE;
+  for (int64_t t = 0; t < T; ++t) {
+    double ss = 0.0;
+    for (int64_t k = 0; k < N; ++k) ss += (double)x[t * N + k] * (double)x[t * N + k];
+    double s = 1.0 / sqrt(ss / (double)N + eps);
+    for (int64_t k = 0; k < N; ++k) y[t * N + k] = ((double)x[t * N + k] * s) * (double)w[k];
+  }
+  return OG_OK;
+}
+
+/* argmax of each row (argmax in qwen3_moe_ssd.js, argmaxRows in qwen35_dense.js): the lowest
+ * index of the largest value.  NaN never compares larger, so it is never picked; a row with
+ * no value other than NaN gives 0. */
+int og_argmax_rows(const double *v, int64_t T, int64_t n, int32_t *ids) {
+  if (T < 0 || n <= 0) return OG_EBADSHAPE;
+  for (int64_t t = 0; t < T; ++t) {
+    int64_t best = -1;
+    for (int64_t i = 0; i < n; ++i) {
+      double a = v[t * n + i];
+      if (isnan(a)) continue;
+      if (best < 0 || a > v[t * n + best]) best = i;
+    }
+    ids[t] = (int32_t)(best < 0 ? 0 : best);
+  }
+  return OG_OK;
+}
