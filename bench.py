@@ -59,7 +59,7 @@ def parse():
                    help="static: the weights are immutable parameters, so each GEMV may start streaming "
                         "them before its predecessor ends (qg_set_static_weights); ordered: every launch "
                         "waits for its predecessor before it reads anything")
-    p.add_argument("--sections", choices=["main", "all", "gemm", "moe", "moe1", "moe8", "kquant", "proj"], default="all",
+    p.add_argument("--sections", choices=["main", "all", "gemm", "moe", "moe1", "moe8", "kquant", "proj", "head"], default="all",
                    help="main: the headline line only; all: plus the detail object; gemm / moe / kquant / "
                         "proj: only that detail section, printed as its own JSON line (for profiling runs)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -352,6 +352,9 @@ def run_section(args):
         res = run_moe(torch, qg, stream, hbm, layers=1, reps=args.steps, warmup=args.warmup, Ts=(8,))
     elif args.sections == "kquant":
         res = run_kquant(torch, qg, stream, hbm, reps=args.steps, warmup=args.warmup)
+    elif args.sections == "head":
+        D = Decode(torch, qg, 1, 1, torch.device("cuda", 0))
+        res = run_head_steps(torch, qg, D, stream, hbm, reps=args.steps, warmup=args.warmup)
     else:
         D = Decode(torch, qg, args.layers, args.tokens, torch.device("cuda", 0))
         res = run_projections(torch, D, stream, hbm, reps=args.steps, warmup=args.warmup)
@@ -525,6 +528,7 @@ def run_detail(torch, qg, D, stream, args, hbm):
         del g
     out["q8_0_T1_per_projection"] = run_projections(torch, D, stream, hbm)
     out["kquant"] = run_kquant(torch, qg, stream, hbm)
+    out["head_steps"] = run_head_steps(torch, qg, D, stream, hbm)
     out["moe_layer"] = run_moe(torch, qg, stream, hbm)
     out["prefill_gemm"] = run_gemm(torch, qg, stream)
     return out
@@ -659,6 +663,52 @@ def run_kquant(torch, qg, stream, hbm, reps=10, warmup=3):
             del g
         del ws, base
     res["Q8_0_1024x1024_T1_batched"] = run_config1_batched(torch, qg, stream, hbm, l2, reps, warmup)
+    return res
+
+
+def run_head_steps(torch, qg, D, stream, hbm, reps=10, warmup=3):
+    """The steps on either side of the GEMV chain: the Gemma-shaped Q6_K tied head 262144 x 2816
+    (606 MB, above L2) alone and with its argmax, the Qwen3 Q8_0 head with its argmax, a
+    16-token embedding gather from the Qwen3 table and the RMSNorm of one token."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    res = {}
+
+    def timed(fn, n_calls):
+        g = capture(torch, fn, stream)
+        el = time_graph(torch, g, stream, reps, warmup)
+        del g
+        return el / (reps * n_calls)
+
+    V6, N6 = 262144, 2816
+    w6 = torch.from_numpy(gs.quant_blocks(gs.Q6_K, V6, N6, seed=0, stream=214)).to(dev)
+    b6 = gs.tensor_bytes(gs.Q6_K, V6, N6)
+    x6 = torch.from_numpy(gs.activations(1, N6, seed=0)).to(dev)
+    lg6 = torch.empty((1, V6), dtype=torch.float32, device=dev)
+    ids = torch.empty(16, dtype=torch.int32, device=dev)
+    t = timed(lambda: [qg.qgemv(gs.Q6_K, w6, x6, V6, N6, lg6) for _ in range(2)], 2)
+    res["q6_k_head_262144x2816_T1"] = {"us": round(t * 1e6, 2), "GB/s": round(b6 / t / 1e9, 1),
+                                       "frac_hbm": round(b6 / t / 1e9 / hbm, 4)}
+    t = timed(lambda: [qg.head_argmax(gs.Q6_K, w6, x6, V6, N6, 1, lg6, ids) for _ in range(2)], 2)
+    res["q6_k_head_argmax_262144x2816_T1"] = {"us": round(t * 1e6, 2), "GB/s": round(b6 / t / 1e9, 1),
+                                              "frac_hbm": round(b6 / t / 1e9 / hbm, 4), "d2h_bytes": 4}
+    del w6
+    M, N = gs.QWEN3_4B_PROJ[HEAD]
+    wh = D.w[HEAD][0]
+    bh = gs.tensor_bytes(gs.Q8_0, M, N)
+    xh = D.x[N]
+    lg = torch.empty((1, M), dtype=torch.float32, device=dev)
+    t = timed(lambda: [qg.head_argmax(gs.Q8_0, wh, xh, M, N, 1, lg, ids) for _ in range(2)], 2)
+    res["q8_0_head_argmax_151936x2560_T1"] = {"us": round(t * 1e6, 2), "GB/s": round(bh / t / 1e9, 1),
+                                              "frac_hbm": round(bh / t / 1e9 / hbm, 4), "d2h_bytes": 4,
+                                              "logits_d2h_bytes_saved": M * 4}
+    tok = torch.from_numpy(np.random.default_rng(0).integers(0, M, 16).astype(np.int32)).to(dev)
+    emb = torch.empty((16, N), dtype=torch.float32, device=dev)
+    t = timed(lambda: [qg.embed_rows(gs.Q8_0, wh, M, N, tok, emb) for _ in range(8)], 8)
+    res["q8_0_embed_16_rows_of_151936x2560"] = {"us": round(t * 1e6, 2), "bytes_read": 16 * gs.row_bytes(gs.Q8_0, N)}
+    wn = torch.ones(N, dtype=torch.float32, device=dev)
+    yn = torch.empty((1, N), dtype=torch.float32, device=dev)
+    t = timed(lambda: [qg.rmsnorm(xh[:1], wn, 1e-6, yn) for _ in range(8)], 8)
+    res["rmsnorm_1x2560"] = {"us": round(t * 1e6, 2)}
     return res
 
 

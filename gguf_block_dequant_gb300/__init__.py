@@ -64,6 +64,10 @@ def load():
             "moe_expert_swiglu": ([I, P, P, I64, P, I, I, P, P, I, I, I, I, P, P, SZ, S], I),
             "moe_combine": ([I, P, I64, P, I, I, P, P, P, I, I, I, I, P, I, P, SZ, S], I),
             "moe_layer": ([I, P, P, P, P, P, I64, P, I, I, I, I, I, I, P, P, P, P, P, SZ, S], I),
+            "qg_embed_rows": ([I, P, I64, I64, P, I, ctypes.c_float, P, S], I),
+            "qg_rmsnorm": ([P, P, I, I64, ctypes.c_float, P, S], I),
+            "qg_argmax_rows": ([P, I, I64, P, S], I),
+            "qg_head_argmax": ([I, P, I64, I64, P, I, P, P, S], I),
         }
         for name, (args, res) in sig.items():
             if hasattr(L, name):
@@ -170,6 +174,33 @@ def qgemv_multi(qtype, ws, ys, x, N, T, stream=None):
     M = (ctypes.c_int64 * n)(*[int(y.shape[-1]) for y in ys])
     _call("qgemv_multi", qtype, n, W, Y, M, N, _ptr(x), T, _stream(stream))
     return ys
+
+
+def embed_rows(qtype, table, V, N, ids, out, scale=1.0, stream=None):
+    """out[i] = scale * dequantized row ids[i] of the [V][N] table (raw blocks)."""
+    _call("qg_embed_rows", qtype, _ptr(table), V, N, _ptr(ids), int(ids.numel()), float(scale), _ptr(out),
+          _stream(stream))
+    return out
+
+
+def rmsnorm(x, w, eps, y, stream=None):
+    """y[t] = x[t] * w / sqrt(mean(x[t]^2) + eps) for x [T][N]."""
+    T, N = (1, x.shape[-1]) if x.dim() == 1 else (x.shape[0], x.shape[1])
+    _call("qg_rmsnorm", _ptr(x), _ptr(w), T, N, float(eps), _ptr(y), _stream(stream))
+    return y
+
+
+def argmax_rows(logits, ids, stream=None):
+    """ids[t] = lowest index of the largest value of logits[t] (NaN never picked)."""
+    T, n = (1, logits.shape[-1]) if logits.dim() == 1 else (logits.shape[0], logits.shape[1])
+    _call("qg_argmax_rows", _ptr(logits), T, n, _ptr(ids), _stream(stream))
+    return ids
+
+
+def head_argmax(qtype, w, x, M, N, T, logits, ids, stream=None):
+    """Tied-head GEMV over T <= 16 tokens into logits [T][M], then ids[t] = argmax logits[t]."""
+    _call("qg_head_argmax", qtype, _ptr(w), M, N, _ptr(x), T, _ptr(logits), _ptr(ids), _stream(stream))
+    return ids
 
 
 def qgemm_workspace_size(qtype, M, N, T) -> int:

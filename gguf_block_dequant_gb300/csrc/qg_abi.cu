@@ -87,7 +87,7 @@ bool set_smem_attr(const void *func, uint32_t bytes) {
 
 extern "C" {
 
-int qg_version(void) { return 2; }
+int qg_version(void) { return 3; }
 
 const char *qg_strerror(int status) {
   switch (status) {
@@ -137,11 +137,17 @@ int qg_set_static_weights(qg_stream_t stream, int enable) {
 qg_status qg_device_status(uint32_t *status_out, int clear) {
   if (!status_out) return QG_EINVAL_PTR;
   if (cudaDeviceSynchronize() != cudaSuccess) return QG_ECUDA;
-  const unsigned int a = qg::read_status_gemv(clear != 0);
-  const unsigned int b = qg::read_status_moe(clear != 0);
-  const unsigned int c = qg::read_status_gemm(clear != 0) | qg::read_status_moetc(clear != 0);
-  if (a == 0xFFFFFFFFu || b == 0xFFFFFFFFu || c == 0xFFFFFFFFu) return QG_ECUDA;
-  *status_out = a | b | c;
+  // one status word per translation unit (device variables are not shared across units)
+  const unsigned int w[] = {qg::read_status_gemv(clear != 0), qg::read_status_gemv1(clear != 0),
+                            qg::read_status_mt(clear != 0),   qg::read_status_head(clear != 0),
+                            qg::read_status_moe(clear != 0),  qg::read_status_gemm(clear != 0),
+                            qg::read_status_moetc(clear != 0)};
+  unsigned int all = 0;
+  for (const unsigned int v : w) {
+    if (v == 0xFFFFFFFFu) return QG_ECUDA;
+    all |= v;
+  }
+  *status_out = all;
   return QG_OK;
 }
 

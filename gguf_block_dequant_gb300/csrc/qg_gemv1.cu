@@ -25,7 +25,7 @@
 #include "qg_host.h"
 #include "qg_pipe.cuh"
 
-extern __device__ unsigned int g_qg_status_gemv;
+__device__ unsigned int g_qg_status_gemv1;  // this translation unit's device status word
 
 namespace {
 
@@ -56,7 +56,7 @@ struct G1Args {
   int early_weights;
 };
 
-QG_DEVICE void g1_status(unsigned int bits) { atomicOr(&g_qg_status_gemv, bits); }
+QG_DEVICE void g1_status(unsigned int bits) { atomicOr(&g_qg_status_gemv1, bits); }
 
 // QT block type, NW warps per CTA, CPS CTAs per SM, RR rows per row block, GU groups per
 // chunk when known at compile time (0: a runtime loop), TT token columns (a.T <= TT of them
@@ -519,6 +519,16 @@ qg_status gemv1_launch(int nmat, const void *const *w, const float *x, float *co
     if (T <= 8) return gemv1_cfg<QT, 8, 1, 2, 8>(nmat, w, x, y, Ms, N, T, stream);
     return gemv1_cfg<QT, 8, 1, 2, 16>(nmat, w, x, y, Ms, N, T, stream);
   }
+}
+
+unsigned int read_status_gemv1(bool clear) {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_qg_status_gemv1, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  if (clear) {
+    const unsigned int z = 0;
+    cudaMemcpyToSymbol(g_qg_status_gemv1, &z, sizeof(z));
+  }
+  return v;
 }
 
 template qg_status gemv1_launch<QG_TYPE_Q8_0>(int, const void *const *, const float *, float *const *, const int64_t *,

@@ -29,7 +29,7 @@
 #include "qg_host.h"
 #include "qg_pipe.cuh"
 
-extern __device__ unsigned int g_qg_status_gemv;
+__device__ unsigned int g_qg_status_mt;  // this translation unit's device status word
 
 namespace {
 
@@ -60,7 +60,7 @@ struct MtArgs {
   int early_weights;
 };
 
-QG_DEVICE void mt_status(unsigned int bits) { atomicOr(&g_qg_status_gemv, bits); }
+QG_DEVICE void mt_status(unsigned int bits) { atomicOr(&g_qg_status_mt, bits); }
 
 QG_DEVICE uint32_t cluster_rank() {
   uint32_t r;
@@ -609,6 +609,16 @@ qg_status gemv_mt_launch(int nmat, const void *const *w, const float *x, float *
     r = gemv_mt_plan<QT, 16>(nmat, w, x, y, Ms, N, T, P);
     return r == QG_OK ? gemv_mt_run<QT, 16>(P, stream) : r;
   }
+}
+
+unsigned int read_status_mt(bool clear) {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_qg_status_mt, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  if (clear) {
+    const unsigned int z = 0;
+    cudaMemcpyToSymbol(g_qg_status_mt, &z, sizeof(z));
+  }
+  return v;
 }
 
 template qg_status gemv_mt_launch<QG_TYPE_Q8_0>(int, const void *const *, const float *, float *const *,

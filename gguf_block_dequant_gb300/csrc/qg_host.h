@@ -82,6 +82,9 @@ qg_status gemv_mt_launch(int nmat, const void *const *w, const float *x, float *
 qg_status gemv_multi_dispatch(int type, int n, const void *const *w, const float *x, float *const *y,
                               const int64_t *M, int64_t N, int T, cudaStream_t s);
 unsigned int read_status_gemv(bool clear);
+unsigned int read_status_gemv1(bool clear);
+unsigned int read_status_mt(bool clear);
+unsigned int read_status_head(bool clear);
 unsigned int read_status_moetc(bool clear);
 unsigned int read_status_moe(bool clear);
 unsigned int read_status_gemm(bool clear);

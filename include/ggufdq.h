@@ -229,6 +229,38 @@ QG_API qg_status moe_layer(int type, const float *xn, const float *wr, const voi
                     int F, int E, int k, int32_t *ids, float *weights, float *act, float *x_inout,
                     void *workspace, size_t workspace_bytes, qg_stream_t stream);
 
+/* ---- the steps on either side of a GEMV chain ----------------------------------------------
+ * Embedding row gather (embedQ8 in qwen3_moe_ssd.js, embedQ6K in gemma4_moe_ssd.js):
+ *   out[i][k] = w(ids[i], k) * scale   for i < n, k < N,
+ * w(r, .) the dequantized row r of the [V][N] table in raw blocks of `type` (any of the four),
+ * decoded by the GEMV's own decoders; the product is one f32 rounding (scale = 1 is exact;
+ * embedQ6K's page multiplies by sqrt(H)).  table: device, 16-byte aligned, V*N/QK blocks;
+ * ids: device int32[n]; out: device f32[n][N], 16-byte aligned.  N a positive multiple of QK,
+ * 1 <= V, 0 <= n (n == 0 enqueues nothing).  An id outside [0, V) gives a zero row and sets
+ * QG_EDEVICE_ID in the device status. */
+QG_API qg_status qg_embed_rows(int type, const void *table, int64_t V, int64_t N, const int32_t *ids, int n,
+                               float scale, float *out, qg_stream_t stream);
+
+/* RMSNorm (rmsnorm in qwen3_moe_ssd.js, rmsnormB for a token batch):
+ *   y[t][k] = (x[t][k] * s_t) * w[k],   s_t = 1 / sqrt(mean_k x[t][k]^2 + eps),
+ * sums in f32.  x, y: device f32[T][N]; w: device f32[N]; all 16-byte aligned; y may be x.
+ * N a positive multiple of 4, 0 <= T <= 65535, eps >= 0. */
+QG_API qg_status qg_rmsnorm(const float *x, const float *w, int T, int64_t N, float eps, float *y, qg_stream_t stream);
+
+/* argmax per row (argmax in qwen3_moe_ssd.js, argmaxRows in qwen35_dense.js): ids[t] = the
+ * lowest index of the largest value of row t of logits[T][n]; NaN is never picked and a row
+ * with nothing but NaN gives 0.  logits, ids: device, 4-byte aligned; 0 <= T <= 8191.  Each
+ * row is scanned by a cluster of 8 CTAs whose partial picks meet in distributed shared memory. */
+QG_API qg_status qg_argmax_rows(const float *logits, int T, int64_t n, int32_t *ids, qg_stream_t stream);
+
+/* Tied head and greedy pick in one call (encodeHead of qwen3_moe_ssd.js: the head GEMV over
+ * the vocabulary, then argmax): logits[t][m] = sum_k W[m][k] * x[t][k] as qgemv_t, then
+ * ids[t] = argmax_m logits[t][m] as qg_argmax_rows.  logits: device f32[T][M] (caller
+ * buffer, written); ids: device int32[T]; 1 <= T <= 16; other rules as qgemv_t.  A caller
+ * that wants only the tokens reads back T ids instead of T * M logits. */
+QG_API qg_status qg_head_argmax(int type, const void *w, int64_t M, int64_t N, const float *x, int T, float *logits,
+                                int32_t *ids, qg_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

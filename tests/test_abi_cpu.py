@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_strings_and_block_shapes(lib):
-    assert lib.qg_version() == 2
+    assert lib.qg_version() == 3
     lib.qg_strerror.restype = ctypes.c_char_p
     assert lib.qg_strerror(0) == b"ok"
     assert lib.qg_strerror(999) == b"unknown status"
@@ -63,6 +63,41 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.qgemv_multi(8, 5, W, Y, M, 64, fake, 1, None) == 1  # n > 4
     assert lib.qgemv_multi(8, 2, W, Y, M, 48, fake, 1, None) == 1  # N % 32 != 0
     assert lib.qgemv_multi(8, 2, None, Y, M, 64, fake, 1, None) == 2
+
+
+def test_head_steps_host_checks_need_no_gpu(lib):
+    P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+    lib.qg_embed_rows.argtypes = [I, P, I64, I64, P, I, F, P, P]
+    lib.qg_rmsnorm.argtypes = [P, P, I, I64, F, P, P]
+    lib.qg_argmax_rows.argtypes = [P, I, I64, P, P]
+    lib.qg_head_argmax.argtypes = [I, P, I64, I64, P, I, P, P, P]
+    fake, odd = P(4096), P(4096 + 2)
+    # embedding gather
+    assert lib.qg_embed_rows(8, None, 4, 64, fake, 1, 1.0, fake, None) == 2
+    assert lib.qg_embed_rows(8, fake, 4, 48, fake, 1, 1.0, fake, None) == 1   # N % 32
+    assert lib.qg_embed_rows(14, fake, 4, 64, fake, 1, 1.0, fake, None) == 1  # N % 256 (Q6_K)
+    assert lib.qg_embed_rows(8, fake, 0, 64, fake, 1, 1.0, fake, None) == 1   # V < 1
+    assert lib.qg_embed_rows(8, fake, 4, 64, fake, -1, 1.0, fake, None) == 1  # n < 0
+    assert lib.qg_embed_rows(8, odd, 4, 64, fake, 1, 1.0, fake, None) == 3    # table alignment
+    assert lib.qg_embed_rows(1, fake, 4, 64, fake, 1, 1.0, fake, None) == 4   # type
+    assert lib.qg_embed_rows(8, fake, 4, 64, fake, 0, 1.0, fake, None) == 0   # n == 0: nothing to do
+    # RMSNorm
+    assert lib.qg_rmsnorm(None, fake, 1, 64, 1e-6, fake, None) == 2
+    assert lib.qg_rmsnorm(fake, fake, 1, 62, 1e-6, fake, None) == 1           # N % 4
+    assert lib.qg_rmsnorm(fake, fake, 1, 64, -1.0, fake, None) == 1           # eps < 0
+    assert lib.qg_rmsnorm(fake, fake, 1, 64, float("nan"), fake, None) == 1
+    assert lib.qg_rmsnorm(fake, odd, 1, 64, 1e-6, fake, None) == 3
+    assert lib.qg_rmsnorm(fake, fake, 0, 64, 1e-6, fake, None) == 0           # T == 0
+    # argmax
+    assert lib.qg_argmax_rows(None, 1, 64, fake, None) == 2
+    assert lib.qg_argmax_rows(fake, 1, 0, fake, None) == 1
+    assert lib.qg_argmax_rows(P(4097), 1, 64, fake, None) == 3
+    # head + argmax: checked in full before the GEMV is enqueued
+    assert lib.qg_head_argmax(8, fake, 64, 64, fake, 1, fake, None, None) == 2
+    assert lib.qg_head_argmax(8, fake, 0, 64, fake, 1, fake, fake, None) == 1
+    assert lib.qg_head_argmax(8, fake, 64, 64, fake, 17, fake, fake, None) == 1
+    assert lib.qg_head_argmax(8, fake, 64, 64, fake, 1, fake, P(4098), None) == 3
+    assert lib.qg_head_argmax(3, fake, 64, 64, fake, 1, fake, fake, None) == 4
 
 
 def test_moe_host_checks_need_no_gpu(lib):
