@@ -66,6 +66,13 @@ def lib():
             L.og_embed_rows.argtypes = [I, P, I64, I64, P, I64, ctypes.c_float, P]
             L.og_rmsnorm.argtypes = [P, P, I64, I64, ctypes.c_double, P]
             L.og_argmax_rows.argtypes = [P, I64, I64, P]
+            L.og_gelu_tanh.argtypes = [ctypes.c_double]
+            L.og_gelu_tanh.restype = ctypes.c_double
+            L.og_sigmoid.argtypes = [ctypes.c_double]
+            L.og_sigmoid.restype = ctypes.c_double
+            L.og_moe_act.argtypes = [I, P, P, I64, P]
+            L.og_moe_combine_ex.argtypes = [P, P, P, P, P, I64, P, P, P, I64, I, I64, I, P, P]
+            L.og_rmsnorm_k.argtypes = [P, P, I64, I64, ctypes.c_double, ctypes.c_double, P]
             _lib = L
     return _lib
 
@@ -218,3 +225,54 @@ def argmax_rows(v: np.ndarray) -> np.ndarray:
     ids = np.empty(v2.shape[0], dtype=np.int32)
     _check(lib().og_argmax_rows(_p(v2), v2.shape[0], v2.shape[1], _p(ids)), "argmax_rows")
     return ids
+
+
+ACT_SILU, ACT_GELU_TANH = 0, 1
+
+
+def gelu_tanh(x: float) -> float:
+    return lib().og_gelu_tanh(float(x))
+
+
+def sigmoid(x: float) -> float:
+    return lib().og_sigmoid(float(x))
+
+
+def moe_act(kind: int, gate: np.ndarray, up: np.ndarray) -> np.ndarray:
+    """act = SiLU(gate) * up (kind 0) or GELU-tanh(gate) * up (kind 1), float64."""
+    g = np.ascontiguousarray(gate, dtype=np.float64)
+    u = np.ascontiguousarray(up, dtype=np.float64)
+    out = np.empty_like(g)
+    _check(lib().og_moe_act(int(kind), _p(g), _p(u), g.size, _p(out)), "moe_act")
+    return out
+
+
+def moe_combine_ex(ids, wts, dn, bound_dn, x_in, k, H, add_residual=1, down_scale=None, E=0, shared_out=None,
+                   shared_gate=None):
+    """out, bound_out [T][H] (float64) of the combine with a per-expert down scale and a
+    sigmoid-gated shared expert, from down rows dn [T*k][H]."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+    T = ids.size // k
+    wts = np.ascontiguousarray(wts, dtype=np.float64).reshape(-1)
+    dn = np.ascontiguousarray(dn, dtype=np.float64).reshape(-1)
+    bdn = None if bound_dn is None else np.ascontiguousarray(bound_dn, dtype=np.float64).reshape(-1)
+    ds = None if down_scale is None else np.ascontiguousarray(down_scale, dtype=np.float32).reshape(-1)
+    sh = None if shared_out is None else np.ascontiguousarray(shared_out, dtype=np.float32).reshape(-1)
+    sg = None if shared_gate is None else np.ascontiguousarray(shared_gate, dtype=np.float32).reshape(-1)
+    x_in = np.ascontiguousarray(x_in, dtype=np.float32).reshape(-1)
+    out = np.empty((T, H), dtype=np.float64)
+    bout = np.empty((T, H), dtype=np.float64)
+    _check(lib().og_moe_combine_ex(_p(ids), _p(wts), _p(dn), _p(bdn), _p(ds), E, _p(sh), _p(sg), _p(x_in), T, k, H,
+                                   int(add_residual), _p(out), _p(bout)), "moe_combine_ex")
+    return out, bout
+
+
+def rmsnorm_k(x: np.ndarray, w: np.ndarray, eps: float, k: float) -> np.ndarray:
+    """y[t][i] = ((x[t][i] * s_t) * k) * w[i], float64 [T][N]."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    x2 = x.reshape(-1, x.shape[-1])
+    w = np.ascontiguousarray(w, dtype=np.float32).reshape(-1)
+    T, N = x2.shape
+    y = np.empty((T, N), dtype=np.float64)
+    _check(lib().og_rmsnorm_k(_p(x2), _p(w), T, N, float(eps), float(k), _p(y)), "rmsnorm_k")
+    return y

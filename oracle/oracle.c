@@ -394,3 +394,77 @@ int og_argmax_rows(const double *v, int64_t T, int64_t n, int32_t *ids) {
   }
   return OG_OK;
 }
+
+/* ---- MoE variants on the same path ------------------------------------------------------ */
+
+/* GELU in the tanh form with the argument clamped to [-10, 10] (GELU / TANH preamble of
+ * gemma4_moe_ssd.js): 0.5 x (1 + tanh(clamp(0.7978845608 x (1 + 0.044715 x^2), -10, 10))). */
+double og_gelu_tanh(double x) {
+  double a = 0.7978845608 * x * (1.0 + 0.044715 * x * x);
+  if (a < -10.0) a = -10.0;
+  if (a > 10.0) a = 10.0;
+  return 0.5 * x * (1.0 + tanh(a));
+}
+
+/* Logistic sigmoid (SIGMOID preamble): 1 / (1 + e^-x). */
+double og_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* Expert activation of gate and up rows: act = SiLU(g) * u (kind 0, siluMulMoe) or
+ * GELU(g) * u (kind 1, geglu). */
+int og_moe_act(int kind, const double *gate, const double *up, int64_t n, double *act) {
+  if (kind != 0 && kind != 1) return OG_EBADSHAPE;
+  for (int64_t i = 0; i < n; ++i)
+    act[i] = kind == 0 ? og_swiglu1(gate[i], up[i]) : og_gelu_tanh(gate[i]) * up[i];
+  return OG_OK;
+}
+
+/* The combine with its variants, from down rows dn [T*k][H] (og_moe_down_combine's):
+ *   acc = sum_j (dn[t*k + j][h] * ds[e_j]) * w[t][j]   in pick order (moeSum; ds = 1 without a
+ *         per-expert down scale, e_j = ids[t*k + j])
+ *   acc = acc + sh[t][h] * sigmoid(sg[t])              with a shared expert (moeAccumShared)
+ *   out[t][h] = acc + (add_residual ? x[t][h] : 0)     the residual last
+ * bound_out = sum_j |ds_j w_j| bound_dn + |sh sigmoid(sg)| + |x|. */
+int og_moe_combine_ex(const int32_t *ids, const double *wts, const double *dn, const double *bound_dn,
+                      const float *down_scale, int64_t E, const float *shared_out, const float *shared_gate,
+                      const float *x_in, int64_t T, int k, int64_t H, int add_residual, double *out,
+                      double *bound_out) {
+  if (T < 0 || k < 1 || H < 1) return OG_EBADSHAPE;
+  for (int64_t t = 0; t < T; ++t) {
+    double g = shared_out ? og_sigmoid((double)shared_gate[t]) : 0.0;
+    for (int64_t h = 0; h < H; ++h) {
+      double acc = 0.0, bnd = 0.0;
+      for (int j = 0; j < k; ++j) {
+        int64_t z = t * k + j;
+        double ds = 1.0;
+        if (down_scale) {
+          if (ids[z] < 0 || ids[z] >= E) return OG_EBADSHAPE;
+          ds = (double)down_scale[ids[z]];
+        }
+        acc = acc + (dn[z * H + h] * ds) * wts[z];
+        if (bound_dn) bnd += fabs(ds * wts[z]) * bound_dn[z * H + h];
+      }
+      if (shared_out) {
+        double sh = (double)shared_out[t * H + h] * g;
+        acc = acc + sh;
+        bnd += fabs(sh);
+      }
+      double xr = add_residual ? (double)x_in[t * H + h] : 0.0;
+      out[t * H + h] = acc + xr;
+      if (bound_out) bound_out[t * H + h] = bnd + fabs(xr);
+    }
+  }
+  return OG_OK;
+}
+
+/* RMSNorm with a factor (rmsnormK of gemma4_moe_ssd.js, the router's input with k = 1/sqrt(H)):
+ *   y[t][i] = ((x[t][i] * s_t) * k) * w[i],   s_t = 1 / sqrt(mean_i x[t][i]^2 + eps). */
+int og_rmsnorm_k(const float *x, const float *w, int64_t T, int64_t N, double eps, double k, double *y) {
+  if (T < 0 || N <= 0) return OG_EBADSHAPE;
+  for (int64_t t = 0; t < T; ++t) {
+    double ss = 0.0;
+    for (int64_t i = 0; i < N; ++i) ss += (double)x[t * N + i] * (double)x[t * N + i];
+    double s = 1.0 / sqrt(ss / (double)N + eps);
+    for (int64_t i = 0; i < N; ++i) y[t * N + i] = (((double)x[t * N + i] * s) * k) * (double)w[i];
+  }
+  return OG_OK;
+}
