@@ -65,7 +65,10 @@ def load():
             "moe_combine": ([I, P, I64, P, I, I, P, P, P, I, I, I, I, P, I, P, SZ, S], I),
             "moe_layer": ([I, P, P, P, P, P, I64, P, I, I, I, I, I, I, P, P, P, P, P, SZ, S], I),
             "qg_embed_rows": ([I, P, I64, I64, P, I, ctypes.c_float, P, S], I),
-            "qg_rmsnorm": ([P, P, I, I64, ctypes.c_float, P, S], I),
+            "qg_rmsnorm": ([P, P, I, I64, ctypes.c_float, ctypes.c_float, P, S], I),
+            "moe_expert_act": ([I, P, P, I64, P, I, I, P, P, I, I, I, I, P, P, P, SZ, S], I),
+            "moe_combine_ex": ([I, P, I64, P, I, I, P, P, P, I, I, I, I, P, P, I, P, SZ, S], I),
+            "moe_layer_ex": ([I, P, P, P, P, P, I64, P, I, I, I, I, I, I, P, P, P, P, P, P, SZ, S], I),
             "qg_argmax_rows": ([P, I, I64, P, S], I),
             "qg_head_argmax": ([I, P, I64, I64, P, I, P, P, S], I),
         }
@@ -183,10 +186,10 @@ def embed_rows(qtype, table, V, N, ids, out, scale=1.0, stream=None):
     return out
 
 
-def rmsnorm(x, w, eps, y, stream=None):
-    """y[t] = x[t] * w / sqrt(mean(x[t]^2) + eps) for x [T][N]."""
+def rmsnorm(x, w, eps, y, k=1.0, stream=None):
+    """y[t] = ((x[t] / sqrt(mean(x[t]^2) + eps)) * k) * w for x [T][N] (k = 1: plain RMSNorm)."""
     T, N = (1, x.shape[-1]) if x.dim() == 1 else (x.shape[0], x.shape[1])
-    _call("qg_rmsnorm", _ptr(x), _ptr(w), T, N, float(eps), _ptr(y), _stream(stream))
+    _call("qg_rmsnorm", _ptr(x), _ptr(w), T, N, float(eps), float(k), _ptr(y), _stream(stream))
     return y
 
 
@@ -248,6 +251,51 @@ def moe_combine(qtype, w_down, expert_stride, slots, n_slots, E, ids, weights, a
     _call("moe_combine", qtype, _ptr(w_down), expert_stride, _ptr(slots), n_slots, E, _ptr(ids), _ptr(weights),
           _ptr(act), T, k, H, F, _ptr(x_inout), int(add_residual), _ptr(workspace), _nbytes(workspace),
           _stream(stream))
+    return x_inout
+
+
+ACT_SILU, ACT_GELU_TANH = 0, 1
+
+
+class MoeVariant(ctypes.Structure):
+    """qg_moe_variant: expert activation, per-expert down scale, sigmoid-gated shared expert."""
+    _fields_ = [("act", ctypes.c_int), ("down_scale", ctypes.c_void_p), ("shared_out", ctypes.c_void_p),
+                ("shared_gate", ctypes.c_void_p)]
+
+
+def moe_variant(act=ACT_SILU, down_scale=None, shared_out=None, shared_gate=None):
+    """A qg_moe_variant from tensors (None for the fields not used).  The struct keeps the
+    tensors alive: it holds their addresses, and the kernels read them when they run."""
+    dp = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    v = MoeVariant(int(act), dp(down_scale), dp(shared_out), dp(shared_gate))
+    v.tensors = (down_scale, shared_out, shared_gate)
+    return v
+
+
+def _var(v):
+    return None if v is None else ctypes.byref(v)
+
+
+def moe_expert_act(qtype, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, variant, act,
+                   workspace=None, stream=None):
+    _call("moe_expert_act", qtype, _ptr(w_gate), _ptr(w_up), expert_stride, _ptr(slots), n_slots, E, _ptr(ids),
+          _ptr(xn), T, k, H, F, _var(variant), _ptr(act), _ptr(workspace), _nbytes(workspace), _stream(stream))
+    return act
+
+
+def moe_combine_ex(qtype, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, variant, x_inout,
+                   add_residual=1, workspace=None, stream=None):
+    _call("moe_combine_ex", qtype, _ptr(w_down), expert_stride, _ptr(slots), n_slots, E, _ptr(ids), _ptr(weights),
+          _ptr(act), T, k, H, F, _var(variant), _ptr(x_inout), int(add_residual), _ptr(workspace),
+          _nbytes(workspace), _stream(stream))
+    return x_inout
+
+
+def moe_layer_ex(qtype, xn, wr, w_gate, w_up, w_down, expert_stride, slots, n_slots, T, H, F, E, k, variant, ids,
+                 weights, act, x_inout, workspace=None, stream=None):
+    _call("moe_layer_ex", qtype, _ptr(xn), _ptr(wr), _ptr(w_gate), _ptr(w_up), _ptr(w_down), expert_stride,
+          _ptr(slots), n_slots, T, H, F, E, k, _var(variant), _ptr(ids), _ptr(weights), _ptr(act), _ptr(x_inout),
+          _ptr(workspace), _nbytes(workspace), _stream(stream))
     return x_inout
 
 

@@ -235,6 +235,15 @@ QG_DEVICE float h2f(uint32_t bits16) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
 }
 
+// Expert activations of gate g and up u: SiLU(g) u (siluMulMoe) and GELU(g) u with the tanh
+// form, its argument clamped to [-10, 10] as the geglu preamble does.
+QG_DEVICE float act_silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+QG_DEVICE float act_gelu_mul(float g, float u) {
+  const float a = fminf(fmaxf(0.7978845608f * g * (1.0f + 0.044715f * g * g), -10.0f), 10.0f);
+  return 0.5f * g * (1.0f + tanhf(a)) * u;
+}
+QG_DEVICE float act_mul(int kind, float g, float u) { return kind ? act_gelu_mul(g, u) : act_silu_mul(g, u); }
+
 QG_DEVICE float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);

@@ -80,9 +80,9 @@ __global__ void __launch_bounds__(kEmbedWarps * 32) embed_kernel(const uint8_t *
   }
 }
 
-// y[t][k] = x[t][k] * s_t * w[k], s_t = 1 / sqrt(mean_k x[t][k]^2 + eps): one CTA per row.
+// y[t][i] = ((x[t][i] * s_t) * k) * w[i], s_t = 1 / sqrt(mean_i x[t][i]^2 + eps): one CTA per row.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float *__restrict__ x, const float *__restrict__ w, int N,
-                                                      float eps, float *__restrict__ y) {
+                                                      float eps, float kf, float *__restrict__ y) {
   __shared__ float part[8];
   const int t = blockIdx.x;
   pdl_wait();
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float *__restrict__ 
   float4 *yr = reinterpret_cast<float4 *>(y + static_cast<size_t>(t) * N);
   for (int i = threadIdx.x; i < n4; i += 256) {
     const float4 v = xr[i], g = wr[i];
-    yr[i] = make_float4((v.x * s) * g.x, (v.y * s) * g.y, (v.z * s) * g.z, (v.w * s) * g.w);
+    yr[i] = make_float4(((v.x * s) * kf) * g.x, ((v.y * s) * kf) * g.y, ((v.z * s) * kf) * g.z, ((v.w * s) * kf) * g.w);
   }
 }
 
@@ -279,13 +279,14 @@ qg_status qg_embed_rows(int type, const void *table, int64_t V, int64_t N, const
   }
 }
 
-qg_status qg_rmsnorm(const float *x, const float *w, int T, int64_t N, float eps, float *y, qg_stream_t stream) {
+qg_status qg_rmsnorm(const float *x, const float *w, int T, int64_t N, float eps, float k, float *y,
+                     qg_stream_t stream) {
   if (!x || !w || !y) return QG_EINVAL_PTR;
-  if (T < 0 || T > 65535 || N <= 0 || N % 4 || N > INT32_MAX || !(eps >= 0.f)) return QG_EINVAL_SHAPE;
+  if (T < 0 || T > 65535 || N <= 0 || N % 4 || N > INT32_MAX || !(eps >= 0.f) || !isfinite(k)) return QG_EINVAL_SHAPE;
   if (!qg::aligned16(x) || !qg::aligned16(w) || !qg::aligned16(y)) return QG_EALIGN;
   if (T == 0) return QG_OK;
   if (qg::launch_pdl(rmsnorm_kernel, dim3(static_cast<unsigned>(T)), dim3(256), 0,
-                     reinterpret_cast<cudaStream_t>(stream), x, w, static_cast<int>(N), eps, y) != cudaSuccess)
+                     reinterpret_cast<cudaStream_t>(stream), x, w, static_cast<int>(N), eps, k, y) != cudaSuccess)
     return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }

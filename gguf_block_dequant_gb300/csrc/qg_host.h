@@ -10,6 +10,15 @@
 
 namespace qg {
 
+// The MoE variants of one call (the header's qg_moe_variant, resolved): expert activation
+// kind, per-expert down scale, sigmoid-gated shared expert.
+struct MoeVar {
+  int act = 0;
+  const float *ds = nullptr;
+  const float *sh = nullptr;
+  const float *sg = nullptr;
+};
+
 struct DeviceInfo {
   bool ok = false;
   int sms = 0;         // streaming multiprocessors
@@ -57,15 +66,16 @@ bool moe_tc_supported(int type, int H, int F, int E);
 size_t moe_tc_workspace(int T, int k, int E, int H, int F);
 qg_status moe_swiglu_tc(const void *w_gate, const void *w_up, int64_t stride, const int32_t *slots, int n_slots,
                         int E, const int32_t *ids, const float *xn, int T, int k, int H, int F, float *act, void *ws,
-                        cudaStream_t s);
-// x[t] = (add_residual ? x[t] : 0) + sum_j w[t][j] dn[t k + j] in pick order, from dn rows in
-// memory (both MoE paths)
+                        cudaStream_t s, int act_kind = 0);
+// x[t] = (add_residual ? x[t] : 0) + [sum_j (dn[t k + j] ds[e_j]) w[t][j] in pick order
+// + sh[t] sigmoid(sg[t])], from dn rows in memory (both MoE paths; ds, sh from v, optional)
 qg_status moe_launch_combine(const float *dn, const float *weights, const int32_t *ids, const int32_t *slots,
                              int n_slots, int E, int T, int k, int H, float *x_inout, int add_residual,
-                             cudaStream_t s);
+                             cudaStream_t s, const MoeVar &v = MoeVar());
 qg_status moe_combine_tc(const void *w_down, int64_t stride, const int32_t *slots, int n_slots, int E,
                          const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
-                         float *x_inout, int add_residual, float *dn, void *ws, cudaStream_t s);
+                         float *x_inout, int add_residual, float *dn, void *ws, cudaStream_t s,
+                         const MoeVar &v = MoeVar());
 
 // GEMV over T <= 16 token columns, lean kernel for rows of 16-byte multiples with resident
 // activations (qg_gemv1.cu); QG_EUNSUPPORTED with nothing launched for other shapes

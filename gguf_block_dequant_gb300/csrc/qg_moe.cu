@@ -196,6 +196,7 @@ struct MoeArgs {
   float *wts_out;
   uint32_t off_plan, off_x, off_ring;
   int plan_only;  // host side: check that the shapes fit the kernel's shared-memory plan, launch nothing
+  int act_kind;   // gate/up: 0 SiLU(g) u (siluMulMoe), 1 GELU-tanh(g) u (geglu)
 };
 
 // Pairs grouped by expert.  s_id[z]: expert of pair z, or -1 when its id or slot is out of
@@ -747,7 +748,7 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const __grid_con
         const bool writer = (NV == 64 || (own && (i0 & 1) == 0));
         if (writer && ok && t < ucnt && i < a.F) {
           const int z = pl.s_pairs[pl.u_first[u] + t];
-          a.out[static_cast<size_t>(z) * a.F + i] = silu_mul(g, uu);
+          a.out[static_cast<size_t>(z) * a.F + i] = act_mul(a.act_kind, g, uu);
         }
       } else {
         const int h0 = RR * p;
@@ -1555,16 +1556,18 @@ MoeArgs swiglu_args(int type, const void *w_gate, const void *w_up, int64_t stri
 qg_status swiglu_impl(int type, const void *w_gate, const void *w_up, int64_t stride, const int32_t *slots,
                       int n_slots, int E, const int32_t *ids, const float *xn, int T, int k, int H, int F,
                       float *act, void *ws, size_t ws_bytes, cudaStream_t s, const float *fused_logits = nullptr,
-                      int32_t *ids_out = nullptr, float *wts_out = nullptr, int plan_only = 0) {
+                      int32_t *ids_out = nullptr, float *wts_out = nullptr, int plan_only = 0,
+                      const qg::MoeVar &v = qg::MoeVar()) {
   const qg_status c = swiglu_check(type, w_gate, w_up, stride, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes);
   if (c != QG_OK) return c;
   if (T > 16) {
     if (plan_only) return QG_OK;
     return qg::moe_swiglu_tc(w_gate, w_up, stride, slots, n_slots, E, ids, xn, T, k, H, F, act,
-                             static_cast<uint8_t *>(ws) + ws_layout(T, k, E, H, F).tc, s);
+                             static_cast<uint8_t *>(ws) + ws_layout(T, k, E, H, F).tc, s, v.act);
   }
   MoeArgs a = swiglu_args(type, w_gate, w_up, stride, slots, n_slots, E, ids, xn, T, k, H, F, act);
   a.plan_only = plan_only;
+  a.act_kind = v.act;
   if (fused_logits) {
     a.fuse_topk = 1;
     a.logits = fused_logits;
@@ -1592,7 +1595,7 @@ qg_status combine_check(int type, const void *w_down, int64_t stride, int n_slot
 qg_status combine_impl(int type, const void *w_down, int64_t stride, const int32_t *slots, int n_slots, int E,
                        const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
                        float *x_inout, int add_residual, void *ws, size_t ws_bytes, cudaStream_t s,
-                       int plan_only = 0) {
+                       int plan_only = 0, const qg::MoeVar &v = qg::MoeVar()) {
   const qg_status c =
       combine_check(type, w_down, stride, n_slots, E, ids, weights, act, T, k, H, F, x_inout, ws, ws_bytes);
   if (c != QG_OK) return c;
@@ -1601,7 +1604,7 @@ qg_status combine_impl(int type, const void *w_down, int64_t stride, const int32
   if (T > 16) {
     if (plan_only) return QG_OK;
     return qg::moe_combine_tc(w_down, stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout,
-                              add_residual ? 1 : 0, reinterpret_cast<float *>(w + L.dn), w + L.tc, s);
+                              add_residual ? 1 : 0, reinterpret_cast<float *>(w + L.dn), w + L.tc, s, v);
   }
   int qk = 0, bb = 0;
   qg_block_shape(type, &qk, &bb);
@@ -1630,7 +1633,24 @@ qg_status combine_impl(int type, const void *w_down, int64_t stride, const int32
   a.plan_only = plan_only;
   const qg_status r = launch_expert_type<true>(type, a, s);
   if (r != QG_OK || plan_only) return r;
-  return qg::moe_launch_combine(a.dn, weights, ids, slots, n_slots, E, T, k, H, x_inout, add_residual ? 1 : 0, s);
+  return qg::moe_launch_combine(a.dn, weights, ids, slots, n_slots, E, T, k, H, x_inout, add_residual ? 1 : 0, s, v);
+}
+
+// The variant of one call: QG_EINVAL_SHAPE for an unknown activation, QG_EINVAL_PTR for a
+// shared row without its gate (or the reverse), QG_EALIGN for misaligned vectors.
+qg_status variant_check(const qg_moe_variant *v, qg::MoeVar &out) {
+  out = qg::MoeVar();
+  if (!v) return QG_OK;
+  if (v->act != QG_ACT_SILU && v->act != QG_ACT_GELU_TANH) return QG_EINVAL_SHAPE;
+  if ((v->shared_out == nullptr) != (v->shared_gate == nullptr)) return QG_EINVAL_PTR;
+  if ((v->shared_out && !qg::aligned16(v->shared_out)) || (reinterpret_cast<uintptr_t>(v->shared_gate) & 3u) ||
+      (reinterpret_cast<uintptr_t>(v->down_scale) & 3u))
+    return QG_EALIGN;
+  out.act = v->act;
+  out.ds = v->down_scale;
+  out.sh = v->shared_out;
+  out.sg = v->shared_gate;
+  return QG_OK;
 }
 
 }  // namespace
@@ -1719,6 +1739,66 @@ qg_status moe_combine(int type, const void *w_down, int64_t expert_stride, const
                       float *x_inout, int add_residual, void *ws, size_t ws_bytes, qg_stream_t stream) {
   return combine_impl(type, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout,
                       add_residual, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qg_status moe_expert_act(int type, const void *w_gate, const void *w_up, int64_t expert_stride,
+                         const int32_t *slots, int n_slots, int E, const int32_t *ids, const float *xn, int T,
+                         int k, int H, int F, const qg_moe_variant *variant, float *act, void *ws,
+                         size_t ws_bytes, qg_stream_t stream) {
+  qg::MoeVar v;
+  const qg_status c = variant_check(variant, v);
+  if (c != QG_OK) return c;
+  return swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes,
+                     reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr, 0, v);
+}
+
+qg_status moe_combine_ex(int type, const void *w_down, int64_t expert_stride, const int32_t *slots, int n_slots,
+                         int E, const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
+                         const qg_moe_variant *variant, float *x_inout, int add_residual, void *ws, size_t ws_bytes,
+                         qg_stream_t stream) {
+  qg::MoeVar v;
+  const qg_status c = variant_check(variant, v);
+  if (c != QG_OK) return c;
+  return combine_impl(type, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout,
+                      add_residual, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), 0, v);
+}
+
+qg_status moe_layer_ex(int type, const float *xn, const float *wr, const void *w_gate, const void *w_up,
+                       const void *w_down, int64_t expert_stride, const int32_t *slots, int n_slots, int T, int H,
+                       int F, int E, int k, const qg_moe_variant *variant, int32_t *ids, float *weights, float *act,
+                       float *x_inout, void *ws, size_t ws_bytes, qg_stream_t stream) {
+  qg::MoeVar v;
+  qg_status c = variant_check(variant, v);
+  if (c != QG_OK) return c;
+  if (v.act == 0 && !v.ds && !v.sh)
+    return moe_layer(type, xn, wr, w_gate, w_up, w_down, expert_stride, slots, n_slots, T, H, F, E, k, ids, weights,
+                     act, x_inout, ws, ws_bytes, stream);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!xn || !wr || !w_gate || !w_up || !w_down || !ids || !weights || !act || !x_inout) return QG_EINVAL_PTR;
+  c = route_check(xn, wr, T, H, E, k, ids, weights);
+  if (c != QG_OK) return c;
+  c = swiglu_check(type, w_gate, w_up, expert_stride, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes);
+  if (c != QG_OK) return c;
+  c = combine_check(type, w_down, expert_stride, n_slots, E, ids, weights, act, T, k, H, F, x_inout, ws, ws_bytes);
+  if (c != QG_OK) return c;
+  if (T <= 16) {
+    // every launch's shared-memory plan before the first launch
+    c = swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes, s,
+                    nullptr, nullptr, nullptr, 1, v);
+    if (c != QG_OK) return c;
+    c = combine_impl(type, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout, 1, ws,
+                     ws_bytes, s, 1, v);
+    if (c != QG_OK) return c;
+  }
+  // the variants run as three steps at every T: router with top-k, expert gate/up with the
+  // variant's activation, down rows and the variant's combine
+  qg_status r = route_impl(xn, wr, T, H, E, k, ids, weights, nullptr, ws, ws_bytes, s, 1);
+  if (r != QG_OK) return r;
+  r = swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes, s,
+                  nullptr, nullptr, nullptr, 0, v);
+  if (r != QG_OK) return r;
+  return combine_impl(type, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout, 1, ws,
+                      ws_bytes, s, 0, v);
 }
 
 qg_status moe_layer(int type, const float *xn, const float *wr, const void *w_gate, const void *w_up,

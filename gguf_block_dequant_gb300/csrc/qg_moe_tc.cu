@@ -146,6 +146,7 @@ struct TcArgs {
   float *act;                 // gate/up: act [P][F] f32
   __nv_bfloat16 *act_sorted;  // gate/up: act in grouped order [P][F] bf16
   float *dn;                  // down: dn [P][H] f32 (row = pair)
+  int act_kind;               // gate/up: 0 SiLU(g) u, 1 GELU-tanh(g) u
 };
 
 QG_DEVICE bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
@@ -351,7 +352,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int col = 16 * cg + c;
             if (col < w.nrows) {
               const float g = v[c], u = s_u[il * U_PITCH + col];
-              const float act = g / (1.0f + expf(-g)) * u;
+              const float act = act_mul(a.act_kind, g, u);
               const int pos = w.row0 + col;
               const int z = a.pl.perm[pos];
               a.act[static_cast<size_t>(z) * a.F + i] = act;
@@ -380,11 +381,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-// x[t][h] = (add_residual ? x[t][h] : 0) + sum_j w[t][j] * dn[t k + j][h], picks in order,
-// picks with a bad id or slot left out
+// x[t][h] = (add_residual ? x[t][h] : 0) + (sum_j (dn[t k + j][h] ds[e_j]) w[t][j] + sh[t][h] s(sg[t])),
+// picks in order (moeAccum; moeSum with the per-expert down scale ds; moeAccumShared with the
+// shared expert's row sh and gate logit sg, s the logistic function), picks with a bad id or
+// slot left out; ds, sh may be null
 __global__ void moe_tc_combine_kernel(const float *__restrict__ dn, const float *__restrict__ wts,
                                       const int32_t *ids, const int32_t *slots, int n_slots, int E, int T, int k,
-                                      int H, float *x, int add_residual) {
+                                      int H, float *x, int add_residual, const float *__restrict__ ds,
+                                      const float *__restrict__ sh, const float *__restrict__ sg) {
   pdl_wait();
   pdl_launch_dependents();
   const int H4 = H / 4;
@@ -398,11 +402,23 @@ __global__ void moe_tc_combine_kernel(const float *__restrict__ dn, const float 
       int e;
       if (!pair_valid(ids, slots, n_slots, E, z, e)) continue;
       const float wj = __ldg(wts + z);
-      const float4 d = __ldg(reinterpret_cast<const float4 *>(dn + static_cast<size_t>(z) * H) + h4);
+      float4 d = __ldg(reinterpret_cast<const float4 *>(dn + static_cast<size_t>(z) * H) + h4);
+      if (ds) {
+        const float c = __ldg(ds + e);
+        d = make_float4(d.x * c, d.y * c, d.z * c, d.w * c);
+      }
       s.x = fmaf(wj, d.x, s.x);
       s.y = fmaf(wj, d.y, s.y);
       s.z = fmaf(wj, d.z, s.z);
       s.w = fmaf(wj, d.w, s.w);
+    }
+    if (sh) {
+      const float gt = 1.0f / (1.0f + expf(-__ldg(sg + t)));
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(sh + static_cast<size_t>(t) * H) + h4);
+      s.x += v.x * gt;
+      s.y += v.y * gt;
+      s.z += v.z * gt;
+      s.w += v.w * gt;
     }
     float4 *xp = reinterpret_cast<float4 *>(x + static_cast<size_t>(t) * H) + h4;
     if (add_residual) {
@@ -527,7 +543,7 @@ size_t moe_tc_workspace(int T, int k, int E, int H, int F) { return tc_layout(T,
 
 qg_status moe_swiglu_tc(const void *w_gate, const void *w_up, int64_t stride, const int32_t *slots, int n_slots,
                         int E, const int32_t *ids, const float *xn, int T, int k, int H, int F, float *act, void *ws,
-                        cudaStream_t s) {
+                        cudaStream_t s, int act_kind) {
   const int P = T * k;
   const TcLayout L = tc_layout(T, k, E, H, F);
   const Plan pl = plan_at(ws, L);
@@ -554,24 +570,26 @@ qg_status moe_swiglu_tc(const void *w_gate, const void *w_up, int64_t stride, co
   a.H = H;
   a.act = act;
   a.act_sorted = acts;
+  a.act_kind = act_kind;
   return launch_tc_gemm<true>(mg, mu, mx, a, s);
 }
 
 qg_status moe_launch_combine(const float *dn, const float *weights, const int32_t *ids, const int32_t *slots,
                              int n_slots, int E, int T, int k, int H, float *x_inout, int add_residual,
-                             cudaStream_t s) {
+                             cudaStream_t s, const MoeVar &v) {
   const qg::DeviceInfo &dev = qg::device_info();
   const long long work = static_cast<long long>(T) * (H / 4);
   const int grid = static_cast<int>(std::max<long long>(1, std::min<long long>(4LL * dev.sms, (work + 127) / 128)));
   return qg::launch_pdl(moe_tc_combine_kernel, dim3(grid), dim3(128), 0, s, dn, weights, ids, slots, n_slots, E, T, k,
-                        H, x_inout, add_residual) == cudaSuccess
+                        H, x_inout, add_residual, v.ds, v.sh, v.sg) == cudaSuccess
              ? QG_OK
              : QG_ECUDA;
 }
 
 qg_status moe_combine_tc(const void *w_down, int64_t stride, const int32_t *slots, int n_slots, int E,
                          const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
-                         float *x_inout, int add_residual, float *dn, void *ws, cudaStream_t s) {
+                         float *x_inout, int add_residual, float *dn, void *ws, cudaStream_t s,
+                         const MoeVar &v) {
   const int P = T * k;
   const TcLayout L = tc_layout(T, k, E, H, F);
   const Plan pl = plan_at(ws, L);
@@ -597,7 +615,7 @@ qg_status moe_combine_tc(const void *w_down, int64_t stride, const int32_t *slot
   a.dn = dn;
   r = launch_tc_gemm<false>(md, md, mx, a, s);
   if (r != QG_OK) return r;
-  return moe_launch_combine(dn, weights, ids, slots, n_slots, E, T, k, H, x_inout, add_residual, s);
+  return moe_launch_combine(dn, weights, ids, slots, n_slots, E, T, k, H, x_inout, add_residual, s, v);
 }
 
 }  // namespace qg

@@ -241,11 +241,13 @@ QG_API qg_status moe_layer(int type, const float *xn, const float *wr, const voi
 QG_API qg_status qg_embed_rows(int type, const void *table, int64_t V, int64_t N, const int32_t *ids, int n,
                                float scale, float *out, qg_stream_t stream);
 
-/* RMSNorm (rmsnorm in qwen3_moe_ssd.js, rmsnormB for a token batch):
- *   y[t][k] = (x[t][k] * s_t) * w[k],   s_t = 1 / sqrt(mean_k x[t][k]^2 + eps),
- * sums in f32.  x, y: device f32[T][N]; w: device f32[N]; all 16-byte aligned; y may be x.
- * N a positive multiple of 4, 0 <= T <= 65535, eps >= 0. */
-QG_API qg_status qg_rmsnorm(const float *x, const float *w, int T, int64_t N, float eps, float *y, qg_stream_t stream);
+/* RMSNorm (rmsnorm in qwen3_moe_ssd.js, rmsnormB for a token batch; with a factor, rmsnormK
+ * of gemma4_moe_ssd.js, the MoE router's input with k = 1/sqrt(H)):
+ *   y[t][i] = ((x[t][i] * s_t) * k) * w[i],   s_t = 1 / sqrt(mean_i x[t][i]^2 + eps),
+ * sums in f32; k = 1 is plain RMSNorm.  x, y: device f32[T][N]; w: device f32[N]; all 16-byte
+ * aligned; y may be x.  N a positive multiple of 4, 0 <= T <= 65535, eps >= 0. */
+QG_API qg_status qg_rmsnorm(const float *x, const float *w, int T, int64_t N, float eps, float k, float *y,
+                            qg_stream_t stream);
 
 /* argmax per row (argmax in qwen3_moe_ssd.js, argmaxRows in qwen35_dense.js): ids[t] = the
  * lowest index of the largest value of row t of logits[T][n]; NaN is never picked and a row
@@ -260,6 +262,46 @@ QG_API qg_status qg_argmax_rows(const float *logits, int T, int64_t n, int32_t *
  * that wants only the tokens reads back T ids instead of T * M logits. */
 QG_API qg_status qg_head_argmax(int type, const void *w, int64_t M, int64_t N, const float *x, int T, float *logits,
                                 int32_t *ids, qg_stream_t stream);
+
+/* ---- MoE variants on the same kernels -----------------------------------------------------
+ * The Gemma 4 MoE (gemma4_moe_ssd.js: Q4_0 experts, geglu, moeSum's per-expert down scale; its
+ * router input is qg_rmsnorm with k = 1/sqrt(H)) and the Qwen3.5/3.6 MoE (qwen35_moe_ssd.js:
+ * moeAccumShared, the sigmoid-gated shared expert) differ from the Qwen3 MoE above only in the
+ * expert activation and the combine.  A variant is a HOST struct; NULL is the Qwen3 MoE. */
+#define QG_ACT_SILU 0      /* act = SiLU(g) * u                         (siluMulMoe) */
+#define QG_ACT_GELU_TANH 1 /* act = GELU(g) * u, tanh form, argument clamped to [-10, 10] (geglu) */
+typedef struct qg_moe_variant {
+  int act;                  /* QG_ACT_SILU or QG_ACT_GELU_TANH */
+  const float *down_scale;  /* NULL, or device f32[E]: pick j's down row is scaled by down_scale[id_j] */
+  const float *shared_out;  /* NULL, or device f32[T][H] (16-byte aligned): the shared expert's output */
+  const float *shared_gate; /* with shared_out: device f32[T], the shared expert's gate logit */
+} qg_moe_variant;
+
+/* moe_expert_swiglu with the variant's activation (act[z][i] = SiLU or GELU of gate, times up). */
+QG_API qg_status moe_expert_act(int type, const void *w_gate, const void *w_up, int64_t expert_stride,
+                                const int32_t *slots, int n_slots, int E, const int32_t *ids, const float *xn, int T,
+                                int k, int H, int F, const qg_moe_variant *variant, float *act, void *workspace,
+                                size_t workspace_bytes, qg_stream_t stream);
+
+/* moe_combine with the variant's combine (moeSum, then moeAccumShared):
+ *   x_inout[t][h] = (add_residual ? x_inout[t][h] : 0)
+ *                   + (sum_j (dn_j[h] * down_scale[id_j]) * weights[t][j]  +  shared_out[t][h] * s(shared_gate[t])),
+ * dn_j = Wd[s_j] . act[t*k + j], s the logistic function, the expert sum in pick order first,
+ * the shared term next, the residual last. */
+QG_API qg_status moe_combine_ex(int type, const void *w_down, int64_t expert_stride, const int32_t *slots,
+                                int n_slots, int E, const int32_t *ids, const float *weights, const float *act, int T,
+                                int k, int H, int F, const qg_moe_variant *variant, float *x_inout, int add_residual,
+                                void *workspace, size_t workspace_bytes, qg_stream_t stream);
+
+/* moe_layer with a variant: router with top-k, moe_expert_act, moe_combine_ex (add_residual =
+ * 1).  A NULL or default variant is moe_layer itself (one launch at T = 1); other variants run
+ * the three steps at every T.  A variant with shared_out and no shared_gate (or the reverse)
+ * returns QG_EINVAL_PTR, an unknown act QG_EINVAL_SHAPE, all before anything is enqueued. */
+QG_API qg_status moe_layer_ex(int type, const float *xn, const float *wr, const void *w_gate, const void *w_up,
+                              const void *w_down, int64_t expert_stride, const int32_t *slots, int n_slots, int T,
+                              int H, int F, int E, int k, const qg_moe_variant *variant, int32_t *ids, float *weights,
+                              float *act, float *x_inout, void *workspace, size_t workspace_bytes,
+                              qg_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -68,7 +68,7 @@ def test_host_argument_checks_need_no_gpu(lib):
 def test_head_steps_host_checks_need_no_gpu(lib):
     P, I, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
     lib.qg_embed_rows.argtypes = [I, P, I64, I64, P, I, F, P, P]
-    lib.qg_rmsnorm.argtypes = [P, P, I, I64, F, P, P]
+    lib.qg_rmsnorm.argtypes = [P, P, I, I64, F, F, P, P]
     lib.qg_argmax_rows.argtypes = [P, I, I64, P, P]
     lib.qg_head_argmax.argtypes = [I, P, I64, I64, P, I, P, P, P]
     fake, odd = P(4096), P(4096 + 2)
@@ -82,12 +82,13 @@ def test_head_steps_host_checks_need_no_gpu(lib):
     assert lib.qg_embed_rows(1, fake, 4, 64, fake, 1, 1.0, fake, None) == 4   # type
     assert lib.qg_embed_rows(8, fake, 4, 64, fake, 0, 1.0, fake, None) == 0   # n == 0: nothing to do
     # RMSNorm
-    assert lib.qg_rmsnorm(None, fake, 1, 64, 1e-6, fake, None) == 2
-    assert lib.qg_rmsnorm(fake, fake, 1, 62, 1e-6, fake, None) == 1           # N % 4
-    assert lib.qg_rmsnorm(fake, fake, 1, 64, -1.0, fake, None) == 1           # eps < 0
-    assert lib.qg_rmsnorm(fake, fake, 1, 64, float("nan"), fake, None) == 1
-    assert lib.qg_rmsnorm(fake, odd, 1, 64, 1e-6, fake, None) == 3
-    assert lib.qg_rmsnorm(fake, fake, 0, 64, 1e-6, fake, None) == 0           # T == 0
+    assert lib.qg_rmsnorm(None, fake, 1, 64, 1e-6, 1.0, fake, None) == 2
+    assert lib.qg_rmsnorm(fake, fake, 1, 62, 1e-6, 1.0, fake, None) == 1           # N % 4
+    assert lib.qg_rmsnorm(fake, fake, 1, 64, -1.0, 1.0, fake, None) == 1           # eps < 0
+    assert lib.qg_rmsnorm(fake, fake, 1, 64, float("nan"), 1.0, fake, None) == 1
+    assert lib.qg_rmsnorm(fake, odd, 1, 64, 1e-6, 1.0, fake, None) == 3
+    assert lib.qg_rmsnorm(fake, fake, 0, 64, 1e-6, 1.0, fake, None) == 0           # T == 0
+    assert lib.qg_rmsnorm(fake, fake, 1, 64, 1e-6, float("inf"), fake, None) == 1  # k not finite
     # argmax
     assert lib.qg_argmax_rows(None, 1, 64, fake, None) == 2
     assert lib.qg_argmax_rows(fake, 1, 0, fake, None) == 1
@@ -130,6 +131,33 @@ def test_moe_host_checks_need_no_gpu(lib):
                                  None) == 4  # unsupported type
     assert lib.moe_combine(8, fake, 0, None, 1, 8, fake, fake, fake, 2, 2, 64, 32, fake, 1, fake, 16,
                            None) == 8  # workspace too small
+
+
+def test_moe_variant_host_checks_need_no_gpu(lib):
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+
+    class Var(ctypes.Structure):
+        _fields_ = [("act", I), ("down_scale", P), ("shared_out", P), ("shared_gate", P)]
+
+    lib.moe_expert_act.argtypes = [I, P, P, I64, P, I, I, P, P, I, I, I, I, P, P, P, SZ, P]
+    lib.moe_combine_ex.argtypes = [I, P, I64, P, I, I, P, P, P, I, I, I, I, P, P, I, P, SZ, P]
+    lib.moe_layer_ex.argtypes = [I, P, P, P, P, P, I64, P, I, I, I, I, I, I, P, P, P, P, P, P, SZ, P]
+    fake = P(4096)
+    bad_act = Var(5, None, None, None)
+    half_shared = Var(0, None, 4096, None)
+    odd_shared = Var(1, None, 4096 + 4, 4096)
+    odd_scale = Var(1, 4096 + 2, None, None)
+    for v, want in ((bad_act, 1), (half_shared, 2), (odd_shared, 3), (odd_scale, 3)):
+        assert lib.moe_expert_act(8, fake, fake, 0, None, 1, 8, fake, fake, 2, 2, 64, 32, ctypes.byref(v), fake,
+                                  fake, 1 << 20, None) == want
+        assert lib.moe_combine_ex(8, fake, 0, None, 1, 8, fake, fake, fake, 2, 2, 64, 32, ctypes.byref(v), fake, 1,
+                                  fake, 1 << 20, None) == want
+        assert lib.moe_layer_ex(4, fake, fake, fake, fake, fake, 0, None, 1, 2, 64, 32, 8, 2, ctypes.byref(v), fake,
+                                fake, fake, fake, fake, 1 << 20, None) == want
+    # a GELU variant goes through the usual shape checks (N % 32 here)
+    gelu = Var(1, None, None, None)
+    assert lib.moe_expert_act(8, fake, fake, 0, None, 1, 8, fake, fake, 2, 2, 48, 32, ctypes.byref(gelu), fake,
+                              fake, 1 << 20, None) == 1
 
 
 def test_moe_rejects_before_enqueueing_anything(lib):
