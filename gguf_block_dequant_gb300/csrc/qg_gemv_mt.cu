@@ -62,6 +62,13 @@ struct MtArgs {
 
 QG_DEVICE void mt_status(unsigned int bits) { atomicOr(&g_qg_status_mt, bits); }
 
+// bytes of one 256-element unit of a row: eight 32-element blocks (Q8_0, Q4_0) or one
+// super-block (Q4_K)
+template <int QT>
+__host__ __device__ constexpr uint32_t unit_bytes() {
+  return QT == QG_TYPE_Q8_0 ? 8u * 34u : QT == QG_TYPE_Q4_0 ? 8u * 18u : 144u;
+}
+
 QG_DEVICE uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -137,9 +144,60 @@ QG_DEVICE void mt_weights(uint32_t row_i, uint32_t row_j, int q, f2 (&w)[2][2][2
   }
 }
 
+// Q4_K: the 16-byte head of a super-block (f16 d, f16 dmin, 12 bytes of packed 6-bit scales
+// and mins) for rows i and i + 8
+struct Q4kHead {
+  float d, dmin;
+  uint32_t s0, s1, s2;  // scale bytes 0-3, 4-7, 8-11
+};
+QG_DEVICE Q4kHead q4k_head(uint32_t blk) {
+  const uint4 v = lds_v4(blk);
+  Q4kHead h;
+  h.d = h2f(v.x & 0xFFFFu);
+  h.dmin = h2f(v.x >> 16);
+  h.s0 = v.y;
+  h.s1 = v.z;
+  h.s2 = v.w;
+  return h;
+}
+QG_DEVICE uint32_t q4k_byte(const Q4kHead &h, int i) {
+  const uint32_t w = i < 4 ? h.s0 : i < 8 ? h.s1 : h.s2;
+  return (w >> (8 * (i & 3))) & 0xFFu;
+}
+// Weights of sub-block SB (elements 32 SB .. 32 SB + 31) of a Q4_K super-block for rows i and
+// i + 8, activation units q and q + 4: w = (d sc) q - dmin m as one fused multiply-add (both
+// products are exact in f32, so this is the single rounding of the exact value).  Sub-block
+// 2c takes the low nibbles of qs[32c ..], 2c + 1 the high ones; its 6-bit scale and min are
+// unpacked from the 12 packed bytes as ggml's get_scale_min_k4 lays them out.
+template <int SB>
+QG_DEVICE void mt_weights_q4k(uint32_t blk_i, uint32_t blk_j, const Q4kHead (&hd)[2], int q, f2 (&w)[2][2][2]) {
+  const uint32_t rows[2] = {blk_i, blk_j};
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    uint32_t sc, mn;
+    if constexpr (SB < 4) {
+      sc = q4k_byte(hd[r], SB) & 63u;
+      mn = q4k_byte(hd[r], SB + 4) & 63u;
+    } else {
+      sc = (q4k_byte(hd[r], SB + 4) & 15u) | ((q4k_byte(hd[r], SB - 4) >> 6) << 4);
+      mn = (q4k_byte(hd[r], SB + 4) >> 4) | ((q4k_byte(hd[r], SB) >> 6) << 4);
+    }
+    const float A = hd[r].d * static_cast<float>(sc), B = hd[r].dmin * static_cast<float>(mn);
+    const f2 A2 = mk2(A, A), nB2 = mk2(-B, -B);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t c = lds_u32(rows[r] + 16u + 32u * (SB >> 1) + 16u * h + 4u * q);
+      f2 a, b;
+      magic4((c >> (4 * (SB & 1))) & 0x0F0F0F0Fu, -8388608.0f, a, b);  // nibble, exactly
+      w[r][h][0] = fma2(a, A2, nB2);
+      w[r][h][1] = fma2(b, A2, nB2);
+    }
+  }
+}
+
 template <int QT, int TT>
 __global__ void __launch_bounds__(kNW * 32, 1) qgemv_mt_kernel(const __grid_constant__ CUtensorMap xmap, const MtArgs a) {
-  constexpr uint32_t BB = QT == QG_TYPE_Q8_0 ? 34u : 18u;
+  constexpr uint32_t UB = unit_bytes<QT>();
   constexpr int TH = TT / 2;  // outputs per lane per group (2 rows x TT tokens over 4 lanes)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -191,12 +249,12 @@ __global__ void __launch_bounds__(kNW * 32, 1) qgemv_mt_kernel(const __grid_cons
     uint32_t row0;
     locate(gA + static_cast<uint32_t>(gl), j, row0);
     const uint32_t nr = min(static_cast<uint32_t>(kRG), a.M[j] - row0);
-    const uint32_t cb = static_cast<uint32_t>(chunk_units(c)) * 8u * BB;
+    const uint32_t cb = static_cast<uint32_t>(chunk_units(c)) * UB;
     if (lane == 0) mbar_arrive_expect_tx(&mybar[s], nr * cb);
     __syncwarp();
     if (static_cast<uint32_t>(lane) < nr)
       bulk_g2s<true>(ring + s * a.stage_bytes + lane * a.seg,
-                     a.w[j] + (row0 + lane) * a.row_bytes + static_cast<uint32_t>(uA + c * a.cbu) * 8u * BB, cb,
+                     a.w[j] + (row0 + lane) * a.row_bytes + static_cast<uint32_t>(uA + c * a.cbu) * UB, cb,
                      &mybar[s]);
   };
 
@@ -265,11 +323,20 @@ __global__ void __launch_bounds__(kNW * 32, 1) qgemv_mt_kernel(const __grid_cons
         uint32_t xb[4];
 #pragma unroll
         for (int m = 0; m < 4; ++m) xb[m] = xu + xq[m];
-        const uint32_t wu = static_cast<uint32_t>(u) * 8u * BB;
+        const uint32_t wu = static_cast<uint32_t>(u) * UB;
+        Q4kHead hd[2];
+        if constexpr (QT == QG_TYPE_Q4_K) {
+          hd[0] = q4k_head(row_i + wu);
+          hd[1] = q4k_head(row_j + wu);
+        }
         auto block = [&](auto blk_c) {
           constexpr int BLK = decltype(blk_c)::value;
           f2 w[2][2][2];
-          mt_weights<QT, BLK>(row_i + wu, row_j + wu, lq, w);
+          if constexpr (QT == QG_TYPE_Q4_K) {
+            mt_weights_q4k<BLK>(row_i + wu, row_j + wu, hd, lq, w);
+          } else {
+            mt_weights<QT, BLK>(row_i + wu, row_j + wu, lq, w);
+          }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             float4 xv[TT];
@@ -485,11 +552,11 @@ long long cluster_fit(int KS) {
 template <int QT, int TT>
 qg_status gemv_mt_plan(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
                        int T, MtPlan &P) {
-  constexpr uint32_t BB = QT == QG_TYPE_Q8_0 ? 34u : 18u;
+  constexpr uint32_t UB = unit_bytes<QT>();
   const DeviceInfo &dev = device_info();
   if (!dev.ok) return QG_ECUDA;
-  if (N % 256 != 0) return QG_EUNSUPPORTED;  // rows of whole 8-block units (16-byte aligned)
-  const long long row_bytes = N / 32 * BB;
+  if (N % 256 != 0) return QG_EUNSUPPORTED;  // rows of whole 256-element units (16-byte aligned)
+  const long long row_bytes = N / 256 * UB;
   MtArgs a{};
   unsigned long long groups = 0;
   for (int j = 0; j < nmat; ++j) {
@@ -522,7 +589,7 @@ qg_status gemv_mt_plan(int nmat, const void *const *w, const float *x, float *co
     const long long gmax = (static_cast<long long>(groups) + ncl - 1) / ncl;
     const long long outs = KS > 1 ? gmax * kRG * TT * 4 : 0;
     for (int cbu : {2, 1}) {
-      const long long seg = static_cast<long long>(cbu) * 8 * BB;
+      const long long seg = static_cast<long long>(cbu) * UB;
       const long long stage = kRG * seg;
       for (int nw : {8, 7}) {
         const long long fixed = 1024 /*alignment*/ + hdr + ((xbytes + 1023) / 1024) * 1024 + ((outs + 1023) / 1024) * 1024;
@@ -592,8 +659,8 @@ qg_status gemv_mt_run(MtPlan &P, cudaStream_t stream) {
 template <int QT>
 qg_status gemv_mt_launch(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
                          int T, cudaStream_t stream) {
-  if constexpr (QT != QG_TYPE_Q8_0 && QT != QG_TYPE_Q4_0) {
-    return QG_EUNSUPPORTED;
+  if constexpr (QT == QG_TYPE_Q6_K) {
+    return QG_EUNSUPPORTED;  // 210-byte super-blocks: rows are not 16-byte multiples
   } else {
     if (T < 2 || T > 16) return QG_EUNSUPPORTED;
     MtPlan P;
