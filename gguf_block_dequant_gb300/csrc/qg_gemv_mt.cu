@@ -36,7 +36,6 @@ namespace {
 constexpr int kNS = 4;     // most slots per warp
 constexpr int kMats = 4;   // matrices per launch (sharing x)
 constexpr int kRG = 16;    // rows per group
-constexpr int kNW = 8;     // most warps per CTA
 
 struct MtArgs {
   const uint8_t *w[kMats];
@@ -195,14 +194,14 @@ QG_DEVICE void mt_weights_q4k(uint32_t blk_i, uint32_t blk_j, const Q4kHead (&hd
   }
 }
 
-template <int QT, int TT>
-__global__ void __launch_bounds__(kNW * 32, 1) qgemv_mt_kernel(const __grid_constant__ CUtensorMap xmap, const MtArgs a) {
+template <int QT, int TT, int NWM>
+__global__ void __launch_bounds__(NWM * 32, 1) qgemv_mt_kernel(const __grid_constant__ CUtensorMap xmap, const MtArgs a) {
   constexpr uint32_t UB = unit_bytes<QT>();
   constexpr int TH = TT / 2;  // outputs per lane per group (2 rows x TT tokens over 4 lanes)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t *wbar = reinterpret_cast<uint64_t *>(smem);  // [kNW][kNS]
-  uint64_t *xfull = wbar + kNW * kNS;
+  uint64_t *wbar = reinterpret_cast<uint64_t *>(smem);  // [NWM][kNS]
+  uint64_t *xfull = wbar + NWM * kNS;
   uint8_t *xs = smem + a.off_x;
 
   const int nw = static_cast<int>(blockDim.x >> 5);
@@ -224,7 +223,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) qgemv_mt_kernel(const __grid_cons
   const int items = warp < NWa ? kb(warp + 1) - k0 : 0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNW * kNS; ++i) mbar_init(&wbar[i], 1);
+    for (int i = 0; i < NWM * kNS; ++i) mbar_init(&wbar[i], 1);
     mbar_init(xfull, 1);
     fence_mbar_init();
   }
@@ -430,7 +429,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) qgemv_mt_kernel(const __grid_cons
     // groups split between warps: parts into slots laid over the (now idle) rings, then warp
     // w, the first boundary inside such a group, sums them in chunk order
     __syncthreads();
-    float *slots = reinterpret_cast<float *>(smem + a.off_ring);  // [2 kNW][32][TH]
+    float *slots = reinterpret_cast<float *>(smem + a.off_ring);  // [2 NWM][32][TH]
     if (held_slot >= 0)
 #pragma unroll
       for (int t = 0; t < TH; ++t) slots[(held_slot * 32 + lane) * TH + t] = held[t];
@@ -518,19 +517,19 @@ struct MtPlan {
 
 // Clusters of KS one-CTA-per-SM CTAs that can be resident at once (a cluster's CTAs share one
 // GPU processing cluster, so this can be below sms / KS); cached per device and KS.
-template <int QT, int TT>
+template <int QT, int TT, int NWM>
 long long cluster_fit(int KS) {
   static long long cache[64][4] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   const int idx = KS == 2 ? 0 : KS == 4 ? 1 : KS == 8 ? 2 : 3;
   if (cache[dev][idx] > 0) return cache[dev][idx];
-  auto kern = qgemv_mt_kernel<QT, TT>;
+  auto kern = qgemv_mt_kernel<QT, TT, NWM>;
   const uint32_t smem = static_cast<uint32_t>(device_info().smem_optin);
   if (!set_smem_attr(reinterpret_cast<const void *>(kern), smem)) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(KS * (device_info().sms / KS)));
-  cfg.blockDim = dim3(kNW * 32);
+  cfg.blockDim = dim3(NWM * 32);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -549,7 +548,7 @@ long long cluster_fit(int KS) {
 }
 
 // Plans the kernel for token tile TT; QG_EUNSUPPORTED when the shape is outside its scope.
-template <int QT, int TT>
+template <int QT, int TT, int NWM>
 qg_status gemv_mt_plan(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
                        int T, MtPlan &P) {
   constexpr uint32_t UB = unit_bytes<QT>();
@@ -584,18 +583,20 @@ qg_status gemv_mt_plan(int nmat, const void *const *w, const float *x, float *co
     const int umax = (a.units + KS - 1) / KS;
     const long long xbytes = static_cast<long long>(TT) * umax * 8 * 128;  // TT token slots per row
     long long ncl = std::min<long long>(dev.sms / KS, static_cast<long long>(groups));
-    if (KS > 1) ncl = std::min<long long>(ncl, cluster_fit<QT, TT>(KS));
+    if (KS > 1) ncl = std::min<long long>(ncl, cluster_fit<QT, TT, NWM>(KS));
     if (ncl < 1) continue;
     const long long gmax = (static_cast<long long>(groups) + ncl - 1) / ncl;
     const long long outs = KS > 1 ? gmax * kRG * TT * 4 : 0;
     for (int cbu : {2, 1}) {
       const long long seg = static_cast<long long>(cbu) * UB;
       const long long stage = kRG * seg;
-      for (int nw : {8, 7}) {
+      const int nws[2] = {NWM == 16 ? 16 : 8, NWM == 16 ? 0 : 7};  // warps per CTA to try
+      for (const int nw : nws) {
+        if (nw == 0) continue;
         const long long fixed = 1024 /*alignment*/ + hdr + ((xbytes + 1023) / 1024) * 1024 + ((outs + 1023) / 1024) * 1024;
         const long long ring_avail = budget - fixed;
         // split-group parts are laid over the rings after the loop
-        const long long parts = 2LL * kNW * 32 * (TT / 2) * 4;
+        const long long parts = 2LL * NWM * 32 * (TT / 2) * 4;
         if (ring_avail < 2LL * nw * stage || ring_avail < parts) continue;
         const int NS = static_cast<int>(std::min<long long>(kNS, ring_avail / (nw * stage)));
         if (NS * nw * stage < parts) continue;
@@ -633,9 +634,9 @@ qg_status gemv_mt_plan(int nmat, const void *const *w, const float *x, float *co
   return QG_EUNSUPPORTED;
 }
 
-template <int QT, int TT>
+template <int QT, int TT, int NWM>
 qg_status gemv_mt_run(MtPlan &P, cudaStream_t stream) {
-  auto kern = qgemv_mt_kernel<QT, TT>;
+  auto kern = qgemv_mt_kernel<QT, TT, NWM>;
   if (!set_smem_attr(reinterpret_cast<const void *>(kern), P.smem)) return QG_ECUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(P.nw * 32);
@@ -666,15 +667,27 @@ qg_status gemv_mt_launch(int nmat, const void *const *w, const float *x, float *
     MtPlan P;
     qg_status r;
     if (T <= 4) {
-      r = gemv_mt_plan<QT, 4>(nmat, w, x, y, Ms, N, T, P);
-      return r == QG_OK ? gemv_mt_run<QT, 4>(P, stream) : r;
+      // up to 4 tokens over fewer than two 16-row groups per SM (the launches this kernel
+      // takes when the lean kernel cannot hold their activations): 16 warps per CTA, whose
+      // rings leave room for only half of K's activations, so K is split over a 2-CTA cluster
+      // (2560 x 9728: 22.9 -> 18.2 us); with more groups 8 warps per CTA are faster
+      // (19456 x 2560: 18.5 vs 20.2 us)
+      long long groups = 0;
+      for (int j = 0; j < nmat; ++j) groups += (Ms[j] + kRG - 1) / kRG;
+      if (groups < 2LL * device_info().sms) {
+        r = gemv_mt_plan<QT, 4, 16>(nmat, w, x, y, Ms, N, T, P);
+        if (r == QG_OK) return gemv_mt_run<QT, 4, 16>(P, stream);
+        if (r != QG_EUNSUPPORTED) return r;
+      }
+      r = gemv_mt_plan<QT, 4, 8>(nmat, w, x, y, Ms, N, T, P);
+      return r == QG_OK ? gemv_mt_run<QT, 4, 8>(P, stream) : r;
     }
     if (T <= 8) {
-      r = gemv_mt_plan<QT, 8>(nmat, w, x, y, Ms, N, T, P);
-      return r == QG_OK ? gemv_mt_run<QT, 8>(P, stream) : r;
+      r = gemv_mt_plan<QT, 8, 8>(nmat, w, x, y, Ms, N, T, P);
+      return r == QG_OK ? gemv_mt_run<QT, 8, 8>(P, stream) : r;
     }
-    r = gemv_mt_plan<QT, 16>(nmat, w, x, y, Ms, N, T, P);
-    return r == QG_OK ? gemv_mt_run<QT, 16>(P, stream) : r;
+    r = gemv_mt_plan<QT, 16, 8>(nmat, w, x, y, Ms, N, T, P);
+    return r == QG_OK ? gemv_mt_run<QT, 16, 8>(P, stream) : r;
   }
 }
 
