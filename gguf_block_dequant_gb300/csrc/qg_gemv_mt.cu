@@ -57,6 +57,7 @@ struct MtArgs {
   int max_groups;           // most row groups of one cluster (KS > 1: size of `outs`)
   uint32_t off_x, off_ring, off_outs;
   int early_weights;
+  uintptr_t mend[kMats];  // Q6_K: last 16-byte boundary of each matrix (its rows are not 16-byte multiples)
 };
 
 QG_DEVICE void mt_status(unsigned int bits) { atomicOr(&g_qg_status_mt, bits); }
@@ -65,7 +66,7 @@ QG_DEVICE void mt_status(unsigned int bits) { atomicOr(&g_qg_status_mt, bits); }
 // super-block (Q4_K)
 template <int QT>
 __host__ __device__ constexpr uint32_t unit_bytes() {
-  return QT == QG_TYPE_Q8_0 ? 8u * 34u : QT == QG_TYPE_Q4_0 ? 8u * 18u : 144u;
+  return QT == QG_TYPE_Q8_0 ? 8u * 34u : QT == QG_TYPE_Q4_0 ? 8u * 18u : QT == QG_TYPE_Q4_K ? 144u : 210u;
 }
 
 QG_DEVICE uint32_t cluster_rank() {
@@ -194,6 +195,40 @@ QG_DEVICE void mt_weights_q4k(uint32_t blk_i, uint32_t blk_j, const Q4kHead (&hd
   }
 }
 
+// 4 bytes at an even shared address (a Q6_K row starts 2-byte aligned in its slot)
+QG_DEVICE uint32_t lds_u32_even(uint32_t addr) {
+  const uint32_t b = addr & ~3u;
+  return __byte_perm(lds_u32(b), lds_u32(b + 4u), (addr & 2u) ? 0x5432u : 0x3210u);
+}
+// Weights of sub-block SB of a Q6_K super-block (ql[128], qh[64], int8 sc[16], f16 d) for rows
+// i and i + 8, activation units q and q + 4.  Element 128 n + 32 qd + l (SB = 4 n + qd) is
+// d * sc[8 n + l / 16 + 2 qd] * (q - 32), q = 4 bits of ql[64 n + 32 (qd & 1) + l] (the low
+// nibble for qd < 2) and 2 bits of qh[32 n + l] at bit 2 qd; (d sc)(q - 32) has at most 23
+// significant bits, so the f32 product is exact.
+template <int SB>
+QG_DEVICE void mt_weights_q6k(uint32_t blk_i, uint32_t blk_j, int q, f2 (&w)[2][2][2]) {
+  constexpr uint32_t n = SB >> 2, qd = SB & 3;
+  const uint32_t rows[2] = {blk_i, blk_j};
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const float d = h2f(lds_u16(rows[r] + 208u));
+    const uint32_t scw = lds_u16(rows[r] + 192u + 8u * n + 2u * qd);
+    const float A[2] = {d * static_cast<float>(static_cast<int8_t>(scw & 0xFFu)),
+                        d * static_cast<float>(static_cast<int8_t>(scw >> 8))};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t lo = lds_u32_even(rows[r] + 64u * n + 32u * (qd & 1u) + 16u * h + 4u * q);
+      const uint32_t hi = lds_u32_even(rows[r] + 128u + 32u * n + 16u * h + 4u * q);
+      const uint32_t qv = ((lo >> (4u * (qd >> 1))) & 0x0F0F0F0Fu) | (((hi >> (2u * qd)) & 0x03030303u) << 4);
+      f2 a, b;
+      magic4(qv, -8388640.0f, a, b);  // q - 32: -(2^23 + 32)
+      const f2 A2 = mk2(A[h], A[h]);
+      w[r][h][0] = mul2(a, A2);
+      w[r][h][1] = mul2(b, A2);
+    }
+  }
+}
+
 template <int QT, int TT, int NWM>
 __global__ void __launch_bounds__(NWM * 32, 1) qgemv_mt_kernel(const __grid_constant__ CUtensorMap xmap, const MtArgs a) {
   constexpr uint32_t UB = unit_bytes<QT>();
@@ -249,12 +284,21 @@ __global__ void __launch_bounds__(NWM * 32, 1) qgemv_mt_kernel(const __grid_cons
     locate(gA + static_cast<uint32_t>(gl), j, row0);
     const uint32_t nr = min(static_cast<uint32_t>(kRG), a.M[j] - row0);
     const uint32_t cb = static_cast<uint32_t>(chunk_units(c)) * UB;
-    if (lane == 0) mbar_arrive_expect_tx(&mybar[s], nr * cb);
-    __syncwarp();
-    if (static_cast<uint32_t>(lane) < nr)
-      bulk_g2s<true>(ring + s * a.stage_bytes + lane * a.seg,
-                     a.w[j] + (row0 + lane) * a.row_bytes + static_cast<uint32_t>(uA + c * a.cbu) * UB, cb,
-                     &mybar[s]);
+    if constexpr (QT == QG_TYPE_Q6_K) {
+      // rows of 210-byte blocks: each row segment is copied from the 16-byte boundary below
+      // it (the slot holds it at its offset from that boundary)
+      const uintptr_t src = reinterpret_cast<uintptr_t>(a.w[j]) + static_cast<uintptr_t>(row0 + lane) * a.row_bytes +
+                            static_cast<uintptr_t>(uA + c * a.cbu) * UB;
+      warp_bulk_copies<true>(ring + s * a.stage_bytes + lane * a.seg, src,
+                             static_cast<uint32_t>(lane) < nr ? cb : 0u, a.mend[j], &mybar[s], lane);
+    } else {
+      if (lane == 0) mbar_arrive_expect_tx(&mybar[s], nr * cb);
+      __syncwarp();
+      if (static_cast<uint32_t>(lane) < nr)
+        bulk_g2s<true>(ring + s * a.stage_bytes + lane * a.seg,
+                       a.w[j] + (row0 + lane) * a.row_bytes + static_cast<uint32_t>(uA + c * a.cbu) * UB, cb,
+                       &mybar[s]);
+    }
   };
 
   int ii = k0 / nc, ic = k0 - (k0 / nc) * nc, is = 0, issued = 0;
@@ -314,7 +358,16 @@ __global__ void __launch_bounds__(NWM * 32, 1) qgemv_mt_kernel(const __grid_cons
     if (ok) {
       ++done;
       const uint32_t st = ring_s + static_cast<uint32_t>(cs) * a.stage_bytes;
-      const uint32_t row_i = st + static_cast<uint32_t>(li) * a.seg, row_j = row_i + 8u * a.seg;
+      uint32_t row_i = st + static_cast<uint32_t>(li) * a.seg, row_j = row_i + 8u * a.seg;
+      if constexpr (QT == QG_TYPE_Q6_K) {
+        // each row sits at its source's offset from a 16-byte boundary
+        int j;
+        uint32_t row0;
+        locate(gA + static_cast<uint32_t>(i), j, row0);
+        const uintptr_t s0 = reinterpret_cast<uintptr_t>(a.w[j]) + static_cast<uintptr_t>(uA + c * a.cbu) * UB;
+        row_i += static_cast<uint32_t>((s0 + static_cast<uintptr_t>(row0 + li) * a.row_bytes) & 15u);
+        row_j += static_cast<uint32_t>((s0 + static_cast<uintptr_t>(row0 + li + 8) * a.row_bytes) & 15u);
+      }
       const int nu = chunk_units(c);
       for (int u = 0; u < nu; ++u) {
         // activation rows of this unit: 8 blocks x TT token slots, from a 1024-byte boundary
@@ -333,6 +386,8 @@ __global__ void __launch_bounds__(NWM * 32, 1) qgemv_mt_kernel(const __grid_cons
           f2 w[2][2][2];
           if constexpr (QT == QG_TYPE_Q4_K) {
             mt_weights_q4k<BLK>(row_i + wu, row_j + wu, hd, lq, w);
+          } else if constexpr (QT == QG_TYPE_Q6_K) {
+            mt_weights_q6k<BLK>(row_i + wu, row_j + wu, lq, w);
           } else {
             mt_weights<QT, BLK>(row_i + wu, row_j + wu, lq, w);
           }
@@ -564,6 +619,7 @@ qg_status gemv_mt_plan(int nmat, const void *const *w, const float *x, float *co
     a.y[j] = y[j];
     a.M[j] = static_cast<uint32_t>(Ms[j]);
     a.rg0[j] = static_cast<uint32_t>(groups);
+    a.mend[j] = (reinterpret_cast<uintptr_t>(w[j]) + static_cast<uintptr_t>(Ms[j] * row_bytes)) & ~static_cast<uintptr_t>(15);
     groups += (Ms[j] + kRG - 1) / kRG;
   }
   if (groups == 0 || groups >= (1ull << 31)) return QG_EUNSUPPORTED;
@@ -588,7 +644,9 @@ qg_status gemv_mt_plan(int nmat, const void *const *w, const float *x, float *co
     const long long gmax = (static_cast<long long>(groups) + ncl - 1) / ncl;
     const long long outs = KS > 1 ? gmax * kRG * TT * 4 : 0;
     for (int cbu : {2, 1}) {
-      const long long seg = static_cast<long long>(cbu) * UB;
+      // Q6_K rows are copied from the 16-byte boundary below them: 16 bytes of slack per row
+      const long long seg = QT == QG_TYPE_Q6_K ? (static_cast<long long>(cbu) * UB + 15) / 16 * 16 + 16
+                                               : static_cast<long long>(cbu) * UB;
       const long long stage = kRG * seg;
       const int nws[2] = {NWM == 16 ? 16 : 8, NWM == 16 ? 0 : 7};  // warps per CTA to try
       for (const int nw : nws) {
@@ -660,9 +718,7 @@ qg_status gemv_mt_run(MtPlan &P, cudaStream_t stream) {
 template <int QT>
 qg_status gemv_mt_launch(int nmat, const void *const *w, const float *x, float *const *y, const int64_t *Ms, int64_t N,
                          int T, cudaStream_t stream) {
-  if constexpr (QT == QG_TYPE_Q6_K) {
-    return QG_EUNSUPPORTED;  // 210-byte super-blocks: rows are not 16-byte multiples
-  } else {
+  {
     if (T < 2 || T > 16) return QG_EUNSUPPORTED;
     MtPlan P;
     qg_status r;

@@ -114,7 +114,7 @@ def test_gemv_one_hot_edge_blocks(qg, oracle_lib, qtype, T, aligned):
             assert np.array_equal(y[t], W[:, k]), (qtype, T, k, np.nonzero(y[t] != W[:, k])[0][:4])
 
 
-@pytest.mark.parametrize("qtype", [gs.Q8_0, gs.Q4_0, gs.Q4_K])
+@pytest.mark.parametrize("qtype", [gs.Q8_0, gs.Q4_0, gs.Q4_K, gs.Q6_K])
 @pytest.mark.parametrize("M,N,T", [(4874, 1024, 4), (4874, 1024, 16), (26, 4096, 16)])
 def test_multi_token_edge_blocks_rows_across_lanes(qg, oracle_lib, qtype, M, N, T):
     """The edge blocks through the rows-across-lanes decoders: 4874 rows are 305 16-row groups
@@ -252,7 +252,7 @@ def test_gemv_multi_matches_separate_calls(qg, oracle_lib, qtype, T):
         assert_within_bound(yd[j].cpu().numpy(), ref, bnd, what=f"multi type {qtype} j={j} T={T}")
 
 
-@pytest.mark.parametrize("qtype", [gs.Q8_0, gs.Q4_0, gs.Q4_K])
+@pytest.mark.parametrize("qtype", [gs.Q8_0, gs.Q4_0, gs.Q4_K, gs.Q6_K])
 @pytest.mark.parametrize("T", [5, 16])
 def test_gemv_multi_rows_across_lanes(qg, oracle_lib, qtype, T):
     """qgemv_multi over 377 16-row groups (the rows-across-lanes kernel goes first), matrices
