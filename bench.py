@@ -59,7 +59,7 @@ def parse():
                    help="static: the weights are immutable parameters, so each GEMV may start streaming "
                         "them before its predecessor ends (qg_set_static_weights); ordered: every launch "
                         "waits for its predecessor before it reads anything")
-    p.add_argument("--sections", choices=["main", "all", "gemm", "moe", "moe1", "moe8", "kquant", "proj", "head"], default="all",
+    p.add_argument("--sections", choices=["main", "all", "gemm", "moe", "moe1", "moe8", "moe512", "kquant", "proj", "head"], default="all",
                    help="main: the headline line only; all: plus the detail object; gemm / moe / kquant / "
                         "proj: only that detail section, printed as its own JSON line (for profiling runs)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -350,6 +350,8 @@ def run_section(args):
         res = run_moe(torch, qg, stream, hbm, layers=1, reps=args.steps, warmup=args.warmup, Ts=(1,))
     elif args.sections == "moe8":  # one expert pool, eight tokens: a small case for profiling
         res = run_moe(torch, qg, stream, hbm, layers=1, reps=args.steps, warmup=args.warmup, Ts=(8,))
+    elif args.sections == "moe512":  # one expert pool, 512 tokens: a small case for profiling
+        res = run_moe(torch, qg, stream, hbm, layers=1, reps=args.steps, warmup=args.warmup, Ts=(512,))
     elif args.sections == "kquant":
         res = run_kquant(torch, qg, stream, hbm, reps=args.steps, warmup=args.warmup)
     elif args.sections == "head":
@@ -606,7 +608,7 @@ def run_moe(torch, qg, stream, hbm, layers=8, reps=50, warmup=3, Ts=(1, 8, 512))
         res[f"T{T}"] = {"us_per_layer": round(us, 2), "unique_experts": round(U, 2),
                         "bytes_per_layer": int(nbytes), "GB/s": round(nbytes / (us * 1e-6) / 1e9, 1),
                         "roofline_us": round(roof_us, 2), "frac_of_roofline": round(roof_us / us, 4),
-                        "launches_per_layer": 1 if T == 1 else 4 if T <= 16 else 8,
+                        "launches_per_layer": 1 if T == 1 else 4 if T <= 16 else 6,
                         "tokens_per_s": round(T / (us * 1e-6), 1),
                         "path": ("one cooperative launch: router, top-k, gate/up, down + combine" if T == 1 else
                                  "CUDA cores, grouped per expert" if T <= 16 else "tcgen05 grouped per expert (bf16)")}

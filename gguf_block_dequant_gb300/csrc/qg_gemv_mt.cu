@@ -645,8 +645,11 @@ qg_status gemv_mt_plan(int nmat, const void *const *w, const float *x, float *co
     const long long outs = KS > 1 ? gmax * kRG * TT * 4 : 0;
     for (int cbu : {2, 1}) {
       // Q6_K rows are copied from the 16-byte boundary below them: 16 bytes of slack per row
-      const long long seg = QT == QG_TYPE_Q6_K ? (static_cast<long long>(cbu) * UB + 15) / 16 * 16 + 16
-                                               : static_cast<long long>(cbu) * UB;
+      long long seg = QT == QG_TYPE_Q6_K ? (static_cast<long long>(cbu) * UB + 15) / 16 * 16 + 16
+                                         : static_cast<long long>(cbu) * UB;
+      // an odd number of 16-byte units per row: the eight rows that a warp reads at one offset
+      // then fall in eight different bank groups (544-byte rows put rows i and i + 4 in one)
+      if ((seg / 16) % 2 == 0) seg += 16;
       const long long stage = kRG * seg;
       const int nws[2] = {NWM == 16 ? 16 : 8, NWM == 16 ? 0 : 7};  // warps per CTA to try
       for (const int nw : nws) {

@@ -75,7 +75,7 @@ qg_status moe_launch_combine(const float *dn, const float *weights, const int32_
 qg_status moe_combine_tc(const void *w_down, int64_t stride, const int32_t *slots, int n_slots, int E,
                          const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
                          float *x_inout, int add_residual, float *dn, void *ws, cudaStream_t s,
-                         const MoeVar &v = MoeVar());
+                         const MoeVar &v = MoeVar(), bool sorted_ready = false);
 
 // GEMV over T <= 16 token columns, lean kernel for rows of 16-byte multiples with resident
 // activations (qg_gemv1.cu); QG_EUNSUPPORTED with nothing launched for other shapes

@@ -162,6 +162,85 @@ __global__ void __launch_bounds__(kRouterWarps * 32) moe_router_kernel(const flo
   if (threadIdx.x == 0) ticket[blockIdx.y] = 0u;
 }
 
+// The same logits for many token tiles: a CTA stages one tile of kRouterTB tokens in shared
+// memory once and runs `epc` experts over it (the kernel above reads the tile from L2 again
+// for every expert: 128 experts x 512 tokens x 8 KB = 537 MB for a 512-token prefill).  Its 16
+// warps are four quads; quad q takes experts eA + q, eA + q + 4, ..., and inside a quad warp w
+// does what warp w of the kernel above does for one expert, so every logit is summed in the
+// same order (lane partials over h = 32 w + lane + 128 j, the warp sum, then the four warp
+// partials in order) and equals that kernel's bit for bit.
+constexpr int kRouterTiledWarps = 16;
+
+__global__ void __launch_bounds__(kRouterTiledWarps * 32, 1)
+    moe_router_tiled_kernel(const float *__restrict__ xn, const float *__restrict__ wr, int T, int H, int E, int k,
+                            int epc, float *logits, int32_t *ids, float *weights, unsigned int *ticket, int do_topk) {
+  extern __shared__ __align__(16) float rt_smem[];
+  float4 *xs = reinterpret_cast<float4 *>(rt_smem);    // [kRouterTB][H / 4]
+  float *part = rt_smem + static_cast<size_t>(kRouterTB) * H;  // [4 quads][kRouterWarps][kRouterTB]
+  __shared__ unsigned int s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quad = warp >> 2, wq = warp & 3;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t0 = blockIdx.y * kRouterTB;
+  const int nt = min(kRouterTB, T - t0);
+  const int H4 = H >> 2;
+  const float4 *xg = reinterpret_cast<const float4 *>(xn + static_cast<size_t>(t0) * H);
+  for (int i = threadIdx.x; i < nt * H4; i += blockDim.x) xs[i] = __ldg(xg + i);
+  __syncthreads();
+  const int eA = blockIdx.x * epc, eB = min(E, eA + epc);
+  float *qpart = part + quad * (kRouterWarps * kRouterTB);
+  for (int e = eA + quad; e < eB; e += 4) {
+    float acc[kRouterTB];
+#pragma unroll
+    for (int t = 0; t < kRouterTB; ++t) acc[t] = 0.f;
+    const float4 *w4 = reinterpret_cast<const float4 *>(wr + static_cast<size_t>(e) * H);
+#pragma unroll 4
+    for (int h = wq * 32 + lane; h < H4; h += kRouterWarps * 32) {
+      const float4 w = __ldg(w4 + h);
+#pragma unroll
+      for (int t = 0; t < kRouterTB; ++t) {
+        if (t < nt) {
+          const float4 x = xs[t * H4 + h];
+          acc[t] = fmaf(w.x, x.x, acc[t]);
+          acc[t] = fmaf(w.y, x.y, acc[t]);
+          acc[t] = fmaf(w.z, x.z, acc[t]);
+          acc[t] = fmaf(w.w, x.w, acc[t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kRouterTB; ++t) {
+      const float s = warp_sum(acc[t]);
+      if (lane == 0) qpart[wq * kRouterTB + t] = s;
+    }
+    named_bar_sync(1 + quad, kRouterWarps * 32);
+    if (wq == 0 && lane < nt) {
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < kRouterWarps; ++w) s += qpart[w * kRouterTB + lane];
+      logits[static_cast<size_t>(t0 + lane) * E + e] = s;
+    }
+    named_bar_sync(1 + quad, kRouterWarps * 32);  // qpart is free for the quad's next expert
+  }
+  if (!do_topk) return;
+  // the last CTA of this token tile to finish takes the picks
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned int old = atomicAdd(&ticket[blockIdx.y], 1u);
+    s_last = (old == gridDim.x - 1) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int t = t0 + warp; t < t0 + nt; t += kRouterTiledWarps)
+    topk_token(logits + static_cast<size_t>(t) * E, E, k, lane, ids + static_cast<size_t>(t) * k,
+               weights + static_cast<size_t>(t) * k);
+  __syncthreads();
+  if (threadIdx.x == 0) ticket[blockIdx.y] = 0u;
+}
+
 // ------------------------------------------------------------------------------------------
 // Expert kernels
 // ------------------------------------------------------------------------------------------
@@ -1265,7 +1344,23 @@ qg_status route_check(const float *xn, const float *wr, int T, int H, int E, int
 // zero again on exit).
 qg_status route_launch(const float *xn, const float *wr, int T, int H, int E, int k, int32_t *ids, float *weights,
                        float *logits, unsigned int *tickets, int do_topk, cudaStream_t s) {
-  const dim3 grid(E, (T + kRouterTB - 1) / kRouterTB);
+  const int tiles = (T + kRouterTB - 1) / kRouterTB;
+  const qg::DeviceInfo &dev = qg::device_info();
+  const size_t tiled_smem = (static_cast<size_t>(kRouterTB) * H + 4 * kRouterWarps * kRouterTB) * 4;
+  if (dev.ok && tiles >= 4 && tiled_smem <= static_cast<size_t>(dev.smem_optin) - 1024) {
+    // many token tiles: each CTA keeps its tile resident and runs a share of the experts,
+    // about one CTA per SM in all
+    const int n_eg = std::max(1, std::min((E + 3) / 4, dev.sms / tiles));
+    const int epc = (E + n_eg - 1) / n_eg;
+    const dim3 grid((E + epc - 1) / epc, tiles);
+    if (!qg::set_smem_attr(reinterpret_cast<const void *>(moe_router_tiled_kernel), static_cast<uint32_t>(tiled_smem)))
+      return QG_ECUDA;
+    if (qg::launch_pdl(moe_router_tiled_kernel, grid, dim3(kRouterTiledWarps * 32), tiled_smem, s, xn, wr, T, H, E, k,
+                       epc, logits, ids, weights, tickets, do_topk) != cudaSuccess)
+      return QG_ECUDA;
+    return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
+  }
+  const dim3 grid(E, tiles);
   if (qg::launch_pdl(moe_router_kernel, grid, dim3(kRouterWarps * 32), 0, s, xn, wr, T, H, E, k, logits, ids, weights,
                      tickets, do_topk) != cudaSuccess)
     return QG_ECUDA;
@@ -1595,7 +1690,7 @@ qg_status combine_check(int type, const void *w_down, int64_t stride, int n_slot
 qg_status combine_impl(int type, const void *w_down, int64_t stride, const int32_t *slots, int n_slots, int E,
                        const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
                        float *x_inout, int add_residual, void *ws, size_t ws_bytes, cudaStream_t s,
-                       int plan_only = 0, const qg::MoeVar &v = qg::MoeVar()) {
+                       int plan_only = 0, const qg::MoeVar &v = qg::MoeVar(), bool sorted_ready = false) {
   const qg_status c =
       combine_check(type, w_down, stride, n_slots, E, ids, weights, act, T, k, H, F, x_inout, ws, ws_bytes);
   if (c != QG_OK) return c;
@@ -1604,7 +1699,7 @@ qg_status combine_impl(int type, const void *w_down, int64_t stride, const int32
   if (T > 16) {
     if (plan_only) return QG_OK;
     return qg::moe_combine_tc(w_down, stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout,
-                              add_residual ? 1 : 0, reinterpret_cast<float *>(w + L.dn), w + L.tc, s, v);
+                              add_residual ? 1 : 0, reinterpret_cast<float *>(w + L.dn), w + L.tc, s, v, sorted_ready);
   }
   int qk = 0, bb = 0;
   qg_block_shape(type, &qk, &bb);
@@ -1797,8 +1892,9 @@ qg_status moe_layer_ex(int type, const float *xn, const float *wr, const void *w
   r = swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes, s,
                   nullptr, nullptr, nullptr, 0, v);
   if (r != QG_OK) return r;
+  // above 16 tokens the gate/up step left the grouping and the sorted act rows for the down step
   return combine_impl(type, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout, 1, ws,
-                      ws_bytes, s, 0, v);
+                      ws_bytes, s, 0, v, T > 16);
 }
 
 qg_status moe_layer(int type, const float *xn, const float *wr, const void *w_gate, const void *w_up,
@@ -1822,7 +1918,7 @@ qg_status moe_layer(int type, const float *xn, const float *wr, const void *w_ga
     r = swiglu_impl(type, w_gate, w_up, expert_stride, slots, n_slots, E, ids, xn, T, k, H, F, act, ws, ws_bytes, s);
     if (r != QG_OK) return r;
     return combine_impl(type, w_down, expert_stride, slots, n_slots, E, ids, weights, act, T, k, H, F, x_inout, 1,
-                        ws, ws_bytes, s);
+                        ws, ws_bytes, s, 0, qg::MoeVar(), true);
   }
   // one token: the whole layer in one cooperative launch when it fits
   if (T == 1) {

@@ -90,18 +90,45 @@ __global__ void __launch_bounds__(1024) moe_tc_plan_kernel(const int32_t *ids, c
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int o = 0, t = 0;
-    for (int e = 0; e < E; ++e) {
-      s_off[e] = o;
-      pl.off[e] = o;
-      pl.toff[e] = t;
-      pl.cnt[e] = s_cnt[e];
-      o += static_cast<int>(s_cnt[e]);
-      t += (static_cast<int>(s_cnt[e]) + BT - 1) / BT;
+  if (threadIdx.x < 32) {
+    // exclusive scans of the pair counts and of the tile counts: lane l holds experts
+    // kMaxE / 32 * l .., the lane totals are scanned with shuffles
+    constexpr int PER = kMaxE / 32;
+    const int lane = threadIdx.x;
+    int c[PER], o_loc = 0, t_loc = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane * PER + i;
+      c[i] = e < E ? static_cast<int>(s_cnt[e]) : 0;
+      o_loc += c[i];
+      t_loc += (c[i] + BT - 1) / BT;
     }
-    pl.off[E] = o;
-    pl.toff[E] = t;
+    int o_inc = o_loc, t_inc = t_loc;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int oa = __shfl_up_sync(0xFFFFFFFFu, o_inc, d), ta = __shfl_up_sync(0xFFFFFFFFu, t_inc, d);
+      if (lane >= d) {
+        o_inc += oa;
+        t_inc += ta;
+      }
+    }
+    int o = o_inc - o_loc, t = t_inc - t_loc;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane * PER + i;
+      if (e < E) {
+        s_off[e] = o;
+        pl.off[e] = o;
+        pl.toff[e] = t;
+        pl.cnt[e] = static_cast<unsigned int>(c[i]);
+      }
+      o += c[i];
+      t += (c[i] + BT - 1) / BT;
+    }
+    if (lane == 31) {
+      pl.off[E] = o_inc;
+      pl.toff[E] = t_inc;
+    }
   }
   __syncthreads();
   for (int z = threadIdx.x; z < P; z += blockDim.x) {
@@ -397,20 +424,36 @@ __global__ void moe_tc_combine_kernel(const float *__restrict__ dn, const float 
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int t = static_cast<int>(i / H4), h4 = static_cast<int>(i - static_cast<long long>(t) * H4);
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-      const int z = t * k + j;
-      int e;
-      if (!pair_valid(ids, slots, n_slots, E, z, e)) continue;
-      const float wj = __ldg(wts + z);
-      float4 d = __ldg(reinterpret_cast<const float4 *>(dn + static_cast<size_t>(z) * H) + h4);
-      if (ds) {
-        const float c = __ldg(ds + e);
-        d = make_float4(d.x * c, d.y * c, d.z * c, d.w * c);
+    // the picks in batches of 8: every dn load of a batch is in flight at once, then the sums
+    // in pick order
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      float4 d[8];
+      float wj[8], c[8];
+      bool use[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int z = t * k + j0 + u;
+        int e = 0;
+        use[u] = j0 + u < k && pair_valid(ids, slots, n_slots, E, z, e);
+        d[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        wj[u] = 0.f;
+        c[u] = 1.f;
+        if (use[u]) {
+          wj[u] = __ldg(wts + z);
+          d[u] = __ldg(reinterpret_cast<const float4 *>(dn + static_cast<size_t>(z) * H) + h4);
+          if (ds) c[u] = __ldg(ds + e);
+        }
       }
-      s.x = fmaf(wj, d.x, s.x);
-      s.y = fmaf(wj, d.y, s.y);
-      s.z = fmaf(wj, d.z, s.z);
-      s.w = fmaf(wj, d.w, s.w);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (!use[u]) continue;
+        float4 v = d[u];
+        if (ds) v = make_float4(v.x * c[u], v.y * c[u], v.z * c[u], v.w * c[u]);
+        s.x = fmaf(wj[u], v.x, s.x);
+        s.y = fmaf(wj[u], v.y, s.y);
+        s.z = fmaf(wj[u], v.z, s.z);
+        s.w = fmaf(wj[u], v.w, s.w);
+      }
     }
     if (sh) {
       const float gt = 1.0f / (1.0f + expf(-__ldg(sg + t)));
@@ -589,7 +632,7 @@ qg_status moe_launch_combine(const float *dn, const float *weights, const int32_
 qg_status moe_combine_tc(const void *w_down, int64_t stride, const int32_t *slots, int n_slots, int E,
                          const int32_t *ids, const float *weights, const float *act, int T, int k, int H, int F,
                          float *x_inout, int add_residual, float *dn, void *ws, cudaStream_t s,
-                         const MoeVar &v) {
+                         const MoeVar &v, bool sorted_ready) {
   const int P = T * k;
   const TcLayout L = tc_layout(T, k, E, H, F);
   const Plan pl = plan_at(ws, L);
@@ -599,10 +642,15 @@ qg_status moe_combine_tc(const void *w_down, int64_t stride, const int32_t *slot
   CUtensorMap md, mx;
   if (!encode_expert_map(&md, w_down, row_bytes, H, n_slots, stride, BM) || !encode_rows_map(&mx, acts, F, P))
     return QG_ECUDA;
-  qg_status r = launch_plan(ids, slots, n_slots, E, P, nullptr, F, pl, s);
-  if (r != QG_OK) return r;
-  r = launch_gather<false>(act, F, k, pl, pl.off + E, acts, P, s);
-  if (r != QG_OK) return r;
+  qg_status r;
+  if (!sorted_ready) {
+    // the grouping and the bf16 act rows in expert order; moe_layer's gate/up step has left
+    // both in the workspace already (its epilogue writes the sorted rows)
+    r = launch_plan(ids, slots, n_slots, E, P, nullptr, F, pl, s);
+    if (r != QG_OK) return r;
+    r = launch_gather<false>(act, F, k, pl, pl.off + E, acts, P, s);
+    if (r != QG_OK) return r;
+  }
   TcArgs a{};
   a.pl = pl;
   a.slots = slots;

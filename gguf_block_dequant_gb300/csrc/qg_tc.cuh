@@ -122,18 +122,13 @@ QG_DEVICE void convert_half(uint32_t raw_row, int sub, int hb, uint32_t a_row, i
   uint32_t d16;
   QG_LDS16(blk, 0, d16);
   const float d = h2f(d16);
+  // the 16 codes start 2-byte aligned: five aligned words and four funnel shifts
   const uint32_t o = blk + 2u + 16u * static_cast<uint32_t>(hb & 1);
-  const uint32_t a16 = o & ~15u, off = o & 15u;
-  const uint4 v0 = lds_v4(a16), v1 = lds_v4(a16 + 16u);
-  const uint64_t q0 = (static_cast<uint64_t>(v0.y) << 32) | v0.x, q1 = (static_cast<uint64_t>(v0.w) << 32) | v0.z;
-  const uint64_t q2 = (static_cast<uint64_t>(v1.y) << 32) | v1.x, q3 = (static_cast<uint64_t>(v1.w) << 32) | v1.z;
-  const bool hi8 = off >= 8u;
-  const uint32_t sh = (off & 7u) * 8u;
-  const uint64_t l0 = hi8 ? q1 : q0, l1 = hi8 ? q2 : q1, l2 = hi8 ? q3 : q2;
-  const uint64_t lo = sh ? (l0 >> sh) | (l1 << (64u - sh)) : l0;
-  const uint64_t hi = sh ? (l1 >> sh) | (l2 << (64u - sh)) : l1;
-  const uint32_t cw[4] = {static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32), static_cast<uint32_t>(hi),
-                          static_cast<uint32_t>(hi >> 32)};
+  const uint32_t wb = o & ~3u, sh = (o & 3u) * 8u;
+  const uint32_t w0 = lds_u32(wb), w1 = lds_u32(wb + 4u), w2 = lds_u32(wb + 8u), w3 = lds_u32(wb + 12u),
+                 w4 = lds_u32(wb + 16u);
+  const uint32_t cw[4] = {__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh), __funnelshift_r(w2, w3, sh),
+                          __funnelshift_r(w3, w4, sh)};
   const f2 d2 = mk2(d, d);
   const f2 bias = mk2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
 #pragma unroll
