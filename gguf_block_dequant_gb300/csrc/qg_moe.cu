@@ -911,8 +911,10 @@ QG_DEVICE void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
 QG_DEVICE bool grid_barrier(unsigned long long *bar, unsigned int nctas, unsigned int *s_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();  // this CTA's writes are visible before its arrival
-    const unsigned long long v = atomicAdd(bar, 1ull);
+    // the arrival is a release: this CTA's writes (ordered before it by the CTA barrier) are
+    // visible to every CTA whose acquire poll sees the count
+    unsigned long long v;
+    asm volatile("atom.release.gpu.global.add.u64 %0, [%1], 1;" : "=l"(v) : "l"(bar) : "memory");
     const unsigned long long target = (v / nctas + 1) * nctas;
     unsigned int ok = 1u;
     const uint64_t t0 = global_ns();
@@ -1077,7 +1079,6 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
       s_base[3 * lane + 2] = reinterpret_cast<uintptr_t>(a.wd) + off;
     }
   }
-  cp_async_wait_all();
   __syncthreads();
   const int kv = static_cast<int>(s_misc[1]);
   // a pick with a bad id has a zero act row
@@ -1186,6 +1187,10 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
     };
     int n_iss = 0;
     for (; ok && n_iss < n_items && n_iss < a.NS - 1; ++n_iss) issue();
+    // the token's activations (copied while the logits arrived) are waited for only now,
+    // after the first weight requests of every warp are out
+    cp_async_wait_all();
+    __syncthreads();
     for (int it = 0; it < n_items && ok; ++it) {
       if (n_iss < n_items) {
         issue();

@@ -31,25 +31,30 @@ namespace {
 
 constexpr int BM = 128;  // weight rows per tile (MMA M)
 constexpr int BT = 64;   // tokens per tile (MMA N)
-constexpr int BK = 64;   // k per operand stage
+constexpr int BK = 64;   // k per MMA step (one 128-byte swizzle atom of bf16)
 constexpr int RK = 256;  // k per raw stage (8 Q8_0 blocks, 272 bytes per row)
-constexpr int NSTAGE = 4;
-constexpr int NRAW = 2;
+// Separate rings per operand: the A slots are filled by the converters from shared memory
+// (short latency: two slots keep them a step ahead of the MMA), the B slots and the raw
+// weight stages come by TMA from L2 and HBM (long latency: deeper rings).
+constexpr int NA = 2;
+constexpr int NB = 8;
+constexpr int NRAW = 3;
 constexpr int NCONV = 16;
-constexpr int NTHREADS = (2 + NCONV) * 32;
+constexpr int NEPI = 4;   // epilogue warps, one per TMEM lane quarter
+constexpr int NTHREADS = (2 + NCONV + NEPI) * 32;
 constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t B_BYTES = BT * BK * 2;
 constexpr uint32_t RAW_ROW = (RK / 32) * 34;
 constexpr uint32_t RAW_BYTES = BM * RAW_ROW;
 constexpr int U_PITCH = BT + 1;  // up-row staging pitch (floats), odd to spread banks
 constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_B = OFF_A + NSTAGE * A_BYTES;
-constexpr uint32_t OFF_RAW = OFF_B + NSTAGE * B_BYTES;
+constexpr uint32_t OFF_B = OFF_A + NA * A_BYTES;
+constexpr uint32_t OFF_RAW = OFF_B + NB * B_BYTES;
 constexpr uint32_t OFF_U = OFF_RAW + NRAW * RAW_BYTES;
 constexpr uint32_t OFF_BAR = OFF_U + ((64 * U_PITCH * 4 + 1023) & ~1023u);
-constexpr uint32_t OFF_TOFF = OFF_BAR + 256;
+constexpr uint32_t OFF_TOFF = OFF_BAR + 512;
 constexpr uint32_t SMEM_BYTES = OFF_TOFF + 260 * 4 + 1024;
-constexpr uint32_t TMEM_COLS = 64;
+constexpr uint32_t TMEM_COLS = 2 * BT;  // two accumulators: a tile's epilogue overlaps the next tile
 constexpr int kMaxE = 256;
 
 struct Plan {
@@ -210,13 +215,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                        const __grid_constant__ CUtensorMap xmap, const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-  uint64_t *empty = full + NSTAGE;
-  uint64_t *rfull = empty + NSTAGE;
+  uint64_t *afull = reinterpret_cast<uint64_t *>(smem + OFF_BAR);  // [NA] converters done
+  uint64_t *aempty = afull + NA;                                     // [NA] MMA done with the slot
+  uint64_t *bfull = aempty + NA;                                     // [NB] B tile landed
+  uint64_t *bempty = bfull + NB;                                     // [NB] MMA done with the slot
+  uint64_t *rfull = bempty + NB;
   uint64_t *rempty = rfull + NRAW;
-  uint64_t *acc_full = rempty + NRAW;
-  uint64_t *acc_empty = acc_full + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
+  uint64_t *acc_full = rempty + NRAW;  // [2]
+  uint64_t *acc_empty = acc_full + 2;  // [2]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_toff = reinterpret_cast<int *>(smem + OFF_TOFF);
   float *s_u = reinterpret_cast<float *>(smem + OFF_U);
@@ -224,16 +231,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = static_cast<int>(gridDim.x);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NSTAGE; ++i) {
-      mbar_init(&full[i], 1 + NCONV);
-      mbar_init(&empty[i], 1);
+    for (int i = 0; i < NA; ++i) {
+      mbar_init(&afull[i], NCONV);
+      mbar_init(&aempty[i], 1);
+    }
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(&bfull[i], 1);
+      mbar_init(&bempty[i], 1);
     }
     for (int i = 0; i < NRAW; ++i) {
       mbar_init(&rfull[i], 1);
       mbar_init(&rempty[i], NCONV);
     }
-    mbar_init(acc_full, 1);
-    mbar_init(acc_empty, NCONV);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], NEPI);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -272,19 +285,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tma_load_3d(raw, &wmap_a, ks * (RK / 32) * 17, w.mt * BM, w.slot, &rfull[r]);
           }
           for (int sub = 0; sub < RK / BK; ++sub, ++st) {
-            const int s = static_cast<int>(st % NSTAGE);
-            if (!tc_wait(&empty[s], static_cast<uint32_t>(((st / NSTAGE) & 1) ^ 1), abort_flag)) {
+            const int s = static_cast<int>(st % NB);
+            if (!tc_wait(&bempty[s], static_cast<uint32_t>(((st / NB) & 1) ^ 1), abort_flag)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[s], B_BYTES);
-            tma_load_2d(smem + OFF_B + s * B_BYTES, &xmap, ks * RK + sub * BK, w.row0, &full[s]);
+            mbar_arrive_expect_tx(&bfull[s], B_BYTES);
+            tma_load_2d(smem + OFF_B + s * B_BYTES, &xmap, ks * RK + sub * BK, w.row0, &bfull[s]);
           }
         }
       }
       if (*abort_flag) {
-        for (long long j = (st > NSTAGE ? st - NSTAGE : 0); j < st; ++j)
-          cleanup_wait(&full[j % NSTAGE], static_cast<uint32_t>((j / NSTAGE) & 1));
+        for (long long j = (st > NB ? st - NB : 0); j < st; ++j)
+          cleanup_wait(&bfull[j % NB], static_cast<uint32_t>((j / NB) & 1));
         for (long long j = (rt > NRAW ? rt - NRAW : 0); j < rt; ++j)
           cleanup_wait(&rfull[j % NRAW], static_cast<uint32_t>((j / NRAW) & 1));
       }
@@ -297,43 +310,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int ii = 0;
       bool ok = true;
       for (long long it = beg; it < end && ok; ++it, ++ii) {
-        if (!tc_wait(acc_empty, static_cast<uint32_t>((ii & 1) ^ 1), abort_flag)) {
+        const int b = ii & 1;  // this tile's accumulator; its previous tile's epilogue must be done
+        if (!tc_wait(&acc_empty[b], static_cast<uint32_t>(((ii >> 1) & 1) ^ 1), abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         for (int ks = 0; ks < a.KS && ok; ++ks) {
           for (int sub = 0; sub < RK / BK; ++sub, ++st) {
-            const int s = static_cast<int>(st % NSTAGE);
-            if (!tc_wait(&full[s], static_cast<uint32_t>((st / NSTAGE) & 1), abort_flag)) {
+            const int sa = static_cast<int>(st % NA), sb = static_cast<int>(st % NB);
+            if (!tc_wait(&bfull[sb], static_cast<uint32_t>((st / NB) & 1), abort_flag) ||
+                !tc_wait(&afull[sa], static_cast<uint32_t>((st / NA) & 1), abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t aa = sA + s * A_BYTES, bb = sB + s * B_BYTES;
+            const uint32_t aa = sA + sa * A_BYTES, bb = sB + sb * B_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
-              tc_mma_bf16(tmem, sw128_desc(aa + kk * 32), sw128_desc(bb + kk * 32), idesc,
-                          (ks == 0 && sub == 0 && kk == 0) ? 0u : 1u);
-            tc_commit(&empty[s]);
+              tc_mma_bf16(tmem + static_cast<uint32_t>(b * BT), sw128_desc(aa + kk * 32), sw128_desc(bb + kk * 32),
+                          idesc, (ks == 0 && sub == 0 && kk == 0) ? 0u : 1u);
+            tc_commit(&aempty[sa]);  // both slots are free once these MMAs finish
+            tc_commit(&bempty[sb]);
           }
         }
-        if (ok) tc_commit(acc_full);
+        if (ok) tc_commit(&acc_full[b]);
       }
-      if (st > 0) cleanup_wait(&empty[(st - 1) % NSTAGE], static_cast<uint32_t>(((st - 1) / NSTAGE) & 1));
+      if (st > 0) cleanup_wait(&bempty[(st - 1) % NB], static_cast<uint32_t>(((st - 1) / NB) & 1));
     }
-  } else {
-    // ---------------- converters, then epilogue ----------------
+  } else if (warp < 2 + NCONV) {
+    // ---------------- converters ----------------
     const int ct = threadIdx.x - 64;
     const int crow = 8 * (ct >> 5) + (lane & 7);
     const int chb = lane >> 3;
-    const int q = warp & 3;
-    const int cg = (warp - 2) >> 2;  // 16 accumulator columns per warp
     long long st = 0, rt = 0;
-    int ii = 0;
     bool ok = true;
-    for (long long it = beg; it < end && ok; ++it, ++ii) {
-      const Item w = item_of(it, a, s_toff);
+    for (long long it = beg; it < end && ok; ++it) {
       for (int ks = 0; ks < a.KS && ok; ++ks, ++rt) {
         const int r = static_cast<int>(rt % NRAW);
         if (!tc_wait(&rfull[r], static_cast<uint32_t>((rt / NRAW) & 1), abort_flag)) {
@@ -341,8 +353,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           break;
         }
         for (int sub = 0; sub < RK / BK; ++sub, ++st) {
-          const int s = static_cast<int>(st % NSTAGE);
-          if (!tc_wait(&empty[s], static_cast<uint32_t>(((st / NSTAGE) & 1) ^ 1), abort_flag)) {
+          const int s = static_cast<int>(st % NA);
+          if (!tc_wait(&aempty[s], static_cast<uint32_t>(((st / NA) & 1) ^ 1), abort_flag)) {
             ok = false;
             break;
           }
@@ -350,55 +362,69 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                        sA + s * A_BYTES + static_cast<uint32_t>(crow) * 128u, crow);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&full[s]);
+          if (lane == 0) mbar_arrive(&afull[s]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&rempty[r]);
       }
-      if (!ok) break;
-      // ---- epilogue of this item
-      if (!tc_wait(acc_full, static_cast<uint32_t>(ii & 1), abort_flag)) {
+    }
+  } else {
+    // ---------------- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 ----------------
+    const int q = warp & 3;
+    int ii = 0;
+    bool ok = true;
+    for (long long it = beg; it < end && ok; ++it, ++ii) {
+      const Item w = item_of(it, a, s_toff);
+      const int b = ii & 1;
+      const bool got = tc_wait(&acc_full[b], static_cast<uint32_t>((ii >> 1) & 1), abort_flag);
+      // the gate/up epilogue's warps meet at named barriers below: they take the abort
+      // decision together, after a barrier that every one of them reaches
+      if (GATEUP) named_bar_sync(1, NEPI * 32);
+      if (!got || *abort_flag) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float v[16];
-      tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(16 * cg), v);
-      if (GATEUP) {
-        // lanes 0-63: gate rows, 64-127: the same up rows
-        const int il = 32 * (q & 1) + lane;
-        if (q >= 2) {
+#pragma unroll 1
+      for (int cg = 0; cg < BT / 16; ++cg) {
+        float v[16];
+        tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BT + 16 * cg), v);
+        if (GATEUP) {
+          // lanes 0-63: gate rows, 64-127: the same up rows
+          const int il = 32 * (q & 1) + lane;
+          if (q >= 2) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) s_u[il * U_PITCH + 16 * cg + c] = v[c];
-        }
-        named_bar_sync(1, NCONV * 32);
-        if (q < 2) {
-          const int i = w.mt * (BM / 2) + il;
+            for (int c = 0; c < 16; ++c) s_u[il * U_PITCH + 16 * cg + c] = v[c];
+          }
+          named_bar_sync(1, NEPI * 32);
+          if (q < 2) {
+            const int i = w.mt * (BM / 2) + il;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int col = 16 * cg + c;
+              if (col < w.nrows) {
+                const float g = v[c], u = s_u[il * U_PITCH + col];
+                const float act = act_mul(a.act_kind, g, u);
+                const int pos = w.row0 + col;
+                const int z = a.pl.perm[pos];
+                a.act[static_cast<size_t>(z) * a.F + i] = act;
+                a.act_sorted[static_cast<size_t>(pos) * a.F + i] = __float2bfloat16_rn(act);
+              }
+            }
+          }
+          named_bar_sync(1, NEPI * 32);  // s_u is free for the next columns
+        } else {
+          const int h = w.mt * BM + 32 * q + lane;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int col = 16 * cg + c;
-            if (col < w.nrows) {
-              const float g = v[c], u = s_u[il * U_PITCH + col];
-              const float act = act_mul(a.act_kind, g, u);
-              const int pos = w.row0 + col;
-              const int z = a.pl.perm[pos];
-              a.act[static_cast<size_t>(z) * a.F + i] = act;
-              a.act_sorted[static_cast<size_t>(pos) * a.F + i] = __float2bfloat16_rn(act);
-            }
+            if (col < w.nrows) a.dn[static_cast<size_t>(a.pl.perm[w.row0 + col]) * a.H + h] = v[c];
           }
-        }
-        named_bar_sync(1, NCONV * 32);  // s_u is free for the next item
-      } else {
-        const int h = w.mt * BM + 32 * q + lane;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int col = 16 * cg + c;
-          if (col < w.nrows) a.dn[static_cast<size_t>(a.pl.perm[w.row0 + col]) * a.H + h] = v[c];
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
+      if (lane == 0) mbar_arrive(&acc_empty[b]);
     }
   }
   __syncthreads();

@@ -115,8 +115,7 @@ QG_DEVICE void cleanup_wait(uint64_t *bar, uint32_t parity) {
 // Decode 16 Q8_0 weights (half hb & 1 of block hb >> 1 of the 64-k stage `sub`) of one row
 // from the raw stage into the A slot.  raw_row: shared address of the row's 272 raw bytes;
 // a_row: shared address of the row in the A slot (128 bytes, 16-byte chunks swizzled by
-// row & 7).  The 16 code bytes are fetched with two aligned 16-byte loads (eight lanes of
-// consecutive rows hit eight different bank groups: the raw row pitch is 17 chunks).
+// row & 7).  The 16 code bytes start 2-byte aligned; they come from five aligned words.
 QG_DEVICE void convert_half(uint32_t raw_row, int sub, int hb, uint32_t a_row, int row) {
   const uint32_t blk = raw_row + 68u * static_cast<uint32_t>(sub) + 34u * static_cast<uint32_t>(hb >> 1);
   uint32_t d16;
