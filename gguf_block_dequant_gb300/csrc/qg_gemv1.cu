@@ -1,6 +1,7 @@
 // qg_gemv1.cu -- one-token quantized GEMV (T = 1), the lean pipeline for the shapes that
-// dominate a decode step: rows whose byte length is a multiple of 16 (every row then starts
-// on a 16-byte boundary) and activations that stay resident in shared memory.
+// dominate a decode step: row blocks whose byte length is a multiple of 16 (every row block
+// then starts on a 16-byte boundary; rows of Q6_K's 210-byte blocks start 2-byte aligned inside
+// them) and activations that stay resident in shared memory.
 //
 // y[m] = sum_k W[m][k] * x[k]  (matmulQ8 / matmulQ4 / the Q4_K row dot of WG_GEMM_Q4K on the
 // engine pages), raw GGUF blocks decoded in registers, f32 accumulation.
@@ -16,7 +17,7 @@
 // What is specialised away, because it cost instruction issue in every stage:
 //   - 32-bit row and byte offsets (every matrix < 4 GiB), matrix bounds precomputed;
 //   - a stage of whole rows is one copy issued by lane 0 alone (rows are contiguous);
-//   - no tail handling of unaligned rows (rows start 16-byte aligned by construction);
+//   - no tail handling of unaligned row blocks (they start 16-byte aligned by construction);
 //   - the item cursor is two counters, the ring slot and phase are counters too.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -356,7 +357,15 @@ qg_status gemv1_plan(int nmat, const void *const *w, const float *x, float *cons
   const DeviceInfo &dev = device_info();
   if (!dev.ok) return QG_ECUDA;
   const long long row_bytes = N / D::QK * D::BB;
-  if (row_bytes % 16 != 0) return QG_EUNSUPPORTED;
+  // rows of a 16-byte multiple, or (Q6_K's 210-byte blocks) row blocks of one: then every
+  // stage holds whole row blocks (one copy from a 16-byte boundary) and every matrix has whole
+  // row blocks, and the decoders read each row at its own 2-byte alignment
+  const bool rows16 = row_bytes % 16 == 0;
+  if (!rows16) {
+    if ((RR * row_bytes) % 16 != 0) return QG_EUNSUPPORTED;
+    for (int j = 0; j < nmat; ++j)
+      if (Ms[j] % RR != 0) return QG_EUNSUPPORTED;
+  }
   const int ngroups = static_cast<int>((N + D::SG - 1) / D::SG);
   const long long xtok = static_cast<long long>(ngroups) * D::SG * 4;
   const long long xres = ((static_cast<long long>(T) * xtok + 1023) / 1024) * 1024;
@@ -418,6 +427,7 @@ qg_status gemv1_plan(int nmat, const void *const *w, const float *x, float *cons
       stage = RR * seg;
     }
   }
+  if (!rows16 && nchunks != 1) return QG_EUNSUPPORTED;  // a chunk of an odd row would not start 16-byte aligned
   NS = static_cast<int>(std::min<long long>(kNS, ring_avail / (static_cast<long long>(NW) * stage)));
   if (NS < 2) return QG_EUNSUPPORTED;
   a.row_bytes = static_cast<uint32_t>(row_bytes);
@@ -501,6 +511,12 @@ qg_status gemv1_launch(int nmat, const void *const *w, const float *x, float *co
     }
     const qg_status r = gemv1_cfg<QT, 8, 2, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
     if (r != QG_EUNSUPPORTED) return r;
+    if constexpr (QT == QG_TYPE_Q6_K) {
+      // Q6_K rows are not 16-byte multiples, so their stages must be whole 2-row blocks: one
+      // 8-warp CTA per SM has the room for two of them per warp
+      const qg_status r6 = gemv1_cfg<QT, 8, 1, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
+      if (r6 != QG_EUNSUPPORTED) return r6;
+    }
     // long rows whose activations leave half an SM too small a ring: one 16-warp CTA per SM
     // holds them once beside a full ring
     return gemv1_cfg<QT, 16, 1, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
