@@ -664,7 +664,8 @@ def run_kquant(torch, qg, stream, hbm, reps=10, warmup=3):
                         "frac_hbm": round(b * n / el / 1e9 / hbm, 4), "copies": R}
             del g
         del ws, base
-    res["Q8_0_1024x1024_T1_batched"] = run_config1_batched(torch, qg, stream, hbm, l2, reps, warmup)
+    res["Q8_0_1024x1024_T1_batched"] = run_batched(torch, qg, stream, hbm, l2, reps, warmup, gs.Q8_0, 1024, 1024, 208)
+    res["Q4_0_2112x2816_T1_batched"] = run_batched(torch, qg, stream, hbm, l2, reps, warmup, gs.Q4_0, 2112, 2816, 209)
     return res
 
 
@@ -714,24 +715,23 @@ def run_head_steps(torch, qg, D, stream, hbm, reps=10, warmup=3):
     return res
 
 
-def run_config1_batched(torch, qg, stream, hbm, l2, reps, warmup):
-    """The 1.1 MB Q8_0 1024x1024 matrix is below what one launch needs to fill HBM: a launch
-    costs about as much as the edges around it.  Independent matrices over the same input in
-    one qgemv_multi launch (4 per launch) show the rate the kernel reaches once the launch
-    edges are shared."""
+def run_batched(torch, qg, stream, hbm, l2, reps, warmup, qt, M, N, sid):
+    """Small matrices (the 1.1 MB Q8_0 1024x1024, the 3.3 MB Q4_0 2112x2816) are below what one
+    launch needs to fill HBM: a launch costs about as much as the edges around it.  Independent
+    matrices over the same input in one qgemv_multi launch (4 per launch) show the rate the
+    kernel reaches once the launch edges are shared."""
     dev = torch.device("cuda", torch.cuda.current_device())
-    M = N = 1024
-    b = gs.tensor_bytes(gs.Q8_0, M, N)
+    b = gs.tensor_bytes(qt, M, N)
     R = max(8, -(-3 * l2 // b))
     R -= R % 4
-    base = torch.from_numpy(gs.quant_blocks(gs.Q8_0, M, N, seed=0, stream=208)).to(dev)
+    base = torch.from_numpy(gs.quant_blocks(qt, M, N, seed=0, stream=sid)).to(dev)
     ws = [base] + [base.clone() for _ in range(R - 1)]
     x = torch.from_numpy(gs.activations(1, N, seed=0)).to(dev)
     ys = [torch.empty((1, M), dtype=torch.float32, device=dev) for _ in range(4)]
 
     def calls():
         for i in range(0, R, 4):
-            qg.qgemv_multi(gs.Q8_0, ws[i:i + 4], ys, x, N, 1)
+            qg.qgemv_multi(qt, ws[i:i + 4], ys, x, N, 1)
     g = capture(torch, calls, stream)
     el = time_graph(torch, g, stream, reps, warmup)
     n = reps * R

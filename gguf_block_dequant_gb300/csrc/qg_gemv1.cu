@@ -55,6 +55,9 @@ struct G1Args {
   int xR, box_rows;
   uint32_t off_x, off_red, off_ring;
   int early_weights;
+  int unal;                  // rows not 16-byte multiples, in chunks: each row's chunk is copied
+                             // from the 16-byte boundary below it and read at its own offset
+  uintptr_t mend[kMats];     // unal: last 16-byte boundary inside each matrix
 };
 
 QG_DEVICE void g1_status(unsigned int bits) { atomicOr(&g_qg_status_gemv1, bits); }
@@ -67,6 +70,7 @@ QG_DEVICE void g1_status(unsigned int bits) { atomicOr(&g_qg_status_gemv1, bits)
 template <int QT, int NW, int CPS, int RR, int GU, int TT, bool XREG = false>
 __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_constant__ CUtensorMap xmap, const G1Args a) {
   using D = Dec<QT>;
+  constexpr bool kUnal = QT == QG_TYPE_Q6_K;  // the only type whose chunked rows may start unaligned
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *wbar = reinterpret_cast<uint64_t *>(smem);  // [NW][kNS]
@@ -127,11 +131,17 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
       }
     } else {
       const uint32_t cb = (c == nc - 1) ? a.row_bytes - static_cast<uint32_t>(c) * a.chunk_bytes : a.chunk_bytes;
-      if (lane == 0) mbar_arrive_expect_tx(&mybar[s], nr * cb);
-      __syncwarp();
-      if (static_cast<uint32_t>(lane) < nr)
-        bulk_g2s<true>(ring + s * a.stage_bytes + lane * a.seg, src + lane * a.row_bytes + static_cast<uint32_t>(c) * a.chunk_bytes,
-                 cb, &mybar[s]);
+      if (kUnal && a.unal) {
+        const uintptr_t sl = reinterpret_cast<uintptr_t>(src) + lane * a.row_bytes + static_cast<uint32_t>(c) * a.chunk_bytes;
+        warp_bulk_copies<true>(ring + s * a.stage_bytes + lane * a.seg, sl, static_cast<uint32_t>(lane) < nr ? cb : 0u,
+                               a.mend[j], &mybar[s], lane);
+      } else {
+        if (lane == 0) mbar_arrive_expect_tx(&mybar[s], nr * cb);
+        __syncwarp();
+        if (static_cast<uint32_t>(lane) < nr)
+          bulk_g2s<true>(ring + s * a.stage_bytes + lane * a.seg, src + lane * a.row_bytes + static_cast<uint32_t>(c) * a.chunk_bytes,
+                   cb, &mybar[s]);
+      }
     }
   };
 
@@ -201,9 +211,20 @@ __global__ void __launch_bounds__(NW * 32, CPS) qgemv1_kernel(const __grid_const
       ++done;
       const uint32_t st = ring_s + static_cast<uint32_t>(cs) * a.stage_bytes + wo;
       const uint32_t pitch = (nc == 1) ? a.row_bytes : a.seg;
+      uint32_t ro[RR];  // each row's offset from the 16-byte boundary its chunk was copied from
+#pragma unroll
+      for (int r = 0; r < RR; ++r) ro[r] = 0u;
+      if (kUnal && a.unal) {
+        int j;
+        uint32_t row;
+        locate(rbA + static_cast<uint32_t>(i), j, row);
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(a.w[j]);
+#pragma unroll
+        for (int r = 0; r < RR; ++r) ro[r] = static_cast<uint32_t>((b0 + (row + r) * static_cast<uintptr_t>(a.row_bytes)) & 15u);
+      }
       RowPrep<QT> rp[RR];
 #pragma unroll
-      for (int r = 0; r < RR; ++r) rp[r].init(st + static_cast<uint32_t>(r) * pitch, lane);
+      for (int r = 0; r < RR; ++r) rp[r].init(st + static_cast<uint32_t>(r) * pitch + ro[r], lane);
       const uint32_t xg0 = xs_s + static_cast<uint32_t>(c * a.gpc) * (D::SG * 4);
       auto group = [&](int g) {
         const uint32_t goff = static_cast<uint32_t>(g * D::GB);
@@ -361,11 +382,6 @@ qg_status gemv1_plan(int nmat, const void *const *w, const float *x, float *cons
   // stage holds whole row blocks (one copy from a 16-byte boundary) and every matrix has whole
   // row blocks, and the decoders read each row at its own 2-byte alignment
   const bool rows16 = row_bytes % 16 == 0;
-  if (!rows16) {
-    if ((RR * row_bytes) % 16 != 0) return QG_EUNSUPPORTED;
-    for (int j = 0; j < nmat; ++j)
-      if (Ms[j] % RR != 0) return QG_EUNSUPPORTED;
-  }
   const int ngroups = static_cast<int>((N + D::SG - 1) / D::SG);
   const long long xtok = static_cast<long long>(ngroups) * D::SG * 4;
   const long long xres = ((static_cast<long long>(T) * xtok + 1023) / 1024) * 1024;
@@ -427,7 +443,32 @@ qg_status gemv1_plan(int nmat, const void *const *w, const float *x, float *cons
       stage = RR * seg;
     }
   }
-  if (!rows16 && nchunks != 1) return QG_EUNSUPPORTED;  // a chunk of an odd row would not start 16-byte aligned
+  if (!rows16) {
+    if (nchunks == 1) {
+      // whole rows: one copy of each row block, which must then be a 16-byte multiple
+      if ((RR * row_bytes) % 16 != 0) return QG_EUNSUPPORTED;
+      for (int j = 0; j < nmat; ++j)
+        if (Ms[j] % RR != 0) return QG_EUNSUPPORTED;
+    } else {
+      // chunks of rows that start anywhere (Q6_K): 16 bytes of slack per row segment, chunks
+      // kept 16-byte multiples, made smaller until two stages per warp fit
+      if (QT != QG_TYPE_Q6_K) return QG_EUNSUPPORTED;
+      a.unal = 1;
+      auto fits = [&]() { return ring_avail / (static_cast<long long>(NW) * RR * (static_cast<long long>(gpc) * D::GB + 16)) >= 2; };
+      while (!fits()) {
+        int g2 = gpc - 1;
+        while (g2 > 0 && (static_cast<long long>(g2) * D::GB) % 16) --g2;
+        if (g2 < 1) return QG_EUNSUPPORTED;
+        gpc = g2;
+      }
+      nchunks = (ngroups + gpc - 1) / gpc;
+      if (nchunks < 2) return QG_EUNSUPPORTED;
+      seg = static_cast<long long>(gpc) * D::GB + 16;
+      stage = RR * seg;
+      for (int j = 0; j < nmat; ++j)
+        a.mend[j] = (reinterpret_cast<uintptr_t>(w[j]) + static_cast<uintptr_t>(Ms[j] * row_bytes)) & ~static_cast<uintptr_t>(15);
+    }
+  }
   NS = static_cast<int>(std::min<long long>(kNS, ring_avail / (static_cast<long long>(NW) * stage)));
   if (NS < 2) return QG_EUNSUPPORTED;
   a.row_bytes = static_cast<uint32_t>(row_bytes);
@@ -509,14 +550,15 @@ qg_status gemv1_launch(int nmat, const void *const *w, const float *x, float *co
         if (r != QG_EUNSUPPORTED) return r;
       }
     }
-    const qg_status r = gemv1_cfg<QT, 8, 2, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
-    if (r != QG_EUNSUPPORTED) return r;
     if constexpr (QT == QG_TYPE_Q6_K) {
-      // Q6_K rows are not 16-byte multiples, so their stages must be whole 2-row blocks: one
-      // 8-warp CTA per SM has the room for two of them per warp
+      // Q6_K rows (210-byte blocks) take one 8-warp CTA per SM: its room holds two whole 2-row
+      // blocks per warp where two CTAs per SM would cut the rows into chunks (17408 x 5120:
+      // 24.1 vs 25.9 us), and longer rows go in realigned chunks
       const qg_status r6 = gemv1_cfg<QT, 8, 1, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
       if (r6 != QG_EUNSUPPORTED) return r6;
     }
+    const qg_status r = gemv1_cfg<QT, 8, 2, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
+    if (r != QG_EUNSUPPORTED) return r;
     // long rows whose activations leave half an SM too small a ring: one 16-warp CTA per SM
     // holds them once beside a full ring
     return gemv1_cfg<QT, 16, 1, 2, 1>(nmat, w, x, y, Ms, N, T, stream);
