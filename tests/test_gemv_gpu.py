@@ -252,6 +252,25 @@ def test_gemv_multi_matches_separate_calls(qg, oracle_lib, qtype, T):
         assert_within_bound(yd[j].cpu().numpy(), ref, bnd, what=f"multi type {qtype} j={j} T={T}")
 
 
+@pytest.mark.parametrize("Ms", [[37, 130, 5], [333]])
+def test_q6k_one_token_rows_at_any_offset(qg, oracle_lib, Ms):
+    """One token over Q6_K rows of 65 super-blocks (13,650 bytes: each row starts 2 bytes further
+    past a 16-byte boundary than the one before, through all eight offsets).  The rows are cut
+    into chunks copied from the boundary below each row and read at the row's own offset; the
+    last row of every matrix ends short of a 16-byte boundary.  Every row against the oracle."""
+    N = 16640
+    x = gs.activations(1, N, seed=11, stream=72)
+    ws = [gs.quant_blocks(gs.Q6_K, M, N, seed=j, stream=90 + j) for j, M in enumerate(Ms)]
+    wd = [to_dev(w, torch) for w in ws]
+    yd = [torch.full((1, M), float("nan"), dtype=torch.float32, device="cuda") for M in Ms]
+    qg.qgemv_multi(gs.Q6_K, wd, yd, to_dev(x, torch), N, 1)
+    torch.cuda.synchronize()
+    assert qg.device_status() == 0
+    for j, M in enumerate(Ms):
+        ref, bnd = oracle_lib.gemv(gs.Q6_K, ws[j], M, N, x, threads=8)
+        assert_within_bound(yd[j].cpu().numpy(), ref, bnd, what=f"Q6_K offsets j={j} M={M}")
+
+
 @pytest.mark.parametrize("qtype", [gs.Q8_0, gs.Q4_0, gs.Q4_K, gs.Q6_K])
 @pytest.mark.parametrize("T", [5, 16])
 def test_gemv_multi_rows_across_lanes(qg, oracle_lib, qtype, T):
