@@ -565,7 +565,9 @@ def run_gemm(torch, qg, stream, reps=10, warmup=3):
         tf = flop / (us * 1e-6) / 1e12
         res[f"q8_0_{M}x{N}_T{T}"] = {"us": round(us, 2), "TFLOP/s": round(tf, 1),
                                      "frac_bf16_peak": round(tf / bf16_peak, 4), "peak_source": src,
-                                     "weight_GB/s": round(b / (us * 1e-6) / 1e9, 1), "launches_per_call": 2}
+                                     "weight_GB/s": round(b / (us * 1e-6) / 1e9, 1),
+                                     # X -> bf16, the GEMM, and (when tiles are split over CTAs) the part sums
+                                     "launches_per_call": 2 if (M // 128) * ((T + 255) // 256) % 152 == 0 else 3}
         del g
     if qg.device_status() != 0:
         raise RuntimeError("device status set in the GEMM benchmark")

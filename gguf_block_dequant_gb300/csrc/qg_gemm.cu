@@ -21,8 +21,8 @@
 //
 // Work split: the (tile, 256-k step) space is cut into equal contiguous ranges, one per CTA
 // (stream-K), so shapes with few tiles and long K still fill every SM.  A tile whose k
-// steps span several CTAs is finished by its last-arriving part, which sums the parts'
-// partial tiles in CTA order (deterministic) and writes Y.
+// steps span several CTAs leaves one partial tile per CTA; a second kernel sums each split
+// tile's parts in CTA order (deterministic) over all SMs at once and writes Y.
 //
 // Every wait is bounded; a wait that expires raises a CTA-wide abort flag so that the other
 // roles stop at their next wait, the status word records QG_ETIMEOUT, in-flight copies and
@@ -57,9 +57,7 @@ constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + NSTAGE * A_BYTES;
 constexpr uint32_t OFF_RAW = OFF_B + NSTAGE * B_BYTES;
 constexpr uint32_t OFF_BAR = OFF_RAW + NRAW * RAW_BYTES;
-constexpr uint32_t OFF_PARTS = OFF_BAR + 256;  // slot list of a split tile's parts
-constexpr int MAX_PARTS = 128;
-constexpr uint32_t SMEM_BYTES = OFF_PARTS + MAX_PARTS * 4 + 1024;  // + alignment slack
+constexpr uint32_t SMEM_BYTES = OFF_BAR + 256 + 1024;  // + alignment slack
 constexpr uint32_t TMEM_COLS = 256;
 
 QG_DEVICE void gemm_status(unsigned int bits) { atomicOr(&g_qg_status_gemm, bits); }
@@ -70,16 +68,15 @@ QG_DEVICE bool wait_or_abort_g(uint64_t *bar, uint32_t parity, volatile int *abo
 struct GemmArgs {
   float *y;
   float *part;           // partial tiles: [2 * gridDim.x][BT][BM]
-  unsigned int *cnt;     // per-tile arrival counters (zeroed by the conversion kernel)
   int M, N, T;
   int n_mt, n_tt, KS;    // m tiles, token tiles, 256-k steps per tile
   long long total;       // tiles * KS
 };
 
 // CTA b's contiguous range of the (tile, k step) space starts at s(b)
-QG_DEVICE long long range_start(long long b, long long total, int G) { return b * total / G; }
+__host__ __device__ inline long long range_start(long long b, long long total, int G) { return b * total / G; }
 // the CTA whose range holds position p
-QG_DEVICE int range_owner(long long p, long long total, int G) {
+__host__ __device__ inline int range_owner(long long p, long long total, int G) {
   return static_cast<int>(((p + 1) * G + total - 1) / total - 1);
 }
 
@@ -96,9 +93,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t *acc_empty = acc_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  volatile unsigned int *s_last = reinterpret_cast<volatile unsigned int *>(tmem_slot + 2);
-  volatile int *s_nparts = reinterpret_cast<volatile int *>(tmem_slot + 3);
-  int *s_parts = reinterpret_cast<int *>(smem + OFF_PARTS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = static_cast<int>(gridDim.x);
@@ -275,79 +269,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
-      if (!whole) {
-        // count this part; the last part of the tile sums all parts in CTA order
-        __threadfence();
-        named_bar_sync(1, NCONV * 32);
-        if (ct == 0) {
-          const long long ts = static_cast<long long>(tile) * a.KS, te = ts + a.KS;
-          const int bf = range_owner(ts, a.total, G), bl = range_owner(te - 1, a.total, G);
-          int parts = 0;
-          for (int bp = bf; bp <= bl; ++bp) {
-            const long long sbp = range_start(bp, a.total, G);
-            if (sbp < range_start(bp + 1, a.total, G)) {
-              if (parts < MAX_PARTS) s_parts[parts] = 2 * bp + (sbp < ts ? 1 : 0);
-              ++parts;
-            }
-          }
-          const unsigned int old = atomicAdd(&a.cnt[tile], 1u);
-          *s_last = (old + 1u == static_cast<unsigned int>(parts)) ? 1u : 0u;
-          *s_nparts = parts;
-        }
-        named_bar_sync(1, NCONV * 32);
-        if (*s_last) {
-          __threadfence();
-          const int parts = *s_nparts;
-          // thread: rows 4 m4 .. 4 m4 + 3, columns cs + NCONV j, in two batches of 8 columns
-          // (8 independent float4 loads in flight per part)
-          const int m4 = ct & 31, cs = ct >> 5;
-          constexpr int NJ = BT / NCONV, NB = 8;
-          const int mg = mt * BM + 4 * m4;
-#pragma unroll 1
-          for (int j0 = 0; j0 < NJ; j0 += NB) {
-            float4 acc[NB];
-#pragma unroll
-            for (int j = 0; j < NB; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int pi = 0; pi < parts; ++pi) {
-              int sl;
-              if (pi < MAX_PARTS) {
-                sl = s_parts[pi];
-              } else {  // more parts than the list holds: recompute this one
-                const long long ts = static_cast<long long>(tile) * a.KS;
-                int bp = range_owner(ts, a.total, G), seen = -1;
-                for (;; ++bp)
-                  if (range_start(bp, a.total, G) < range_start(bp + 1, a.total, G) && ++seen == pi) break;
-                sl = 2 * bp + (range_start(bp, a.total, G) < ts ? 1 : 0);
-              }
-              const float4 *pp = reinterpret_cast<const float4 *>(a.part + static_cast<size_t>(sl) * BT * BM);
-#pragma unroll
-              for (int j = 0; j < NB; ++j) {
-                const float4 v = __ldcg(pp + (cs + NCONV * (j0 + j)) * (BM / 4) + m4);
-                acc[j].x += v.x;
-                acc[j].y += v.y;
-                acc[j].z += v.z;
-                acc[j].w += v.w;
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < NB; ++j) {
-              const int t = tt * BT + cs + NCONV * (j0 + j);
-              if (t >= a.T) continue;
-              float *yr = a.y + static_cast<size_t>(t) * a.M;
-              if (mg + 3 < a.M && (a.M & 3) == 0) {
-                *reinterpret_cast<float4 *>(yr + mg) = acc[j];
-              } else {
-                if (mg < a.M) yr[mg] = acc[j].x;
-                if (mg + 1 < a.M) yr[mg + 1] = acc[j].y;
-                if (mg + 2 < a.M) yr[mg + 2] = acc[j].z;
-                if (mg + 3 < a.M) yr[mg + 3] = acc[j].w;
-              }
-            }
-          }
-          named_bar_sync(1, NCONV * 32);
-          if (ct == 0) a.cnt[tile] = 0u;
-        }
-      }
       pos += k1 - k0;
     }
   }
@@ -359,9 +280,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-// f32 -> bf16 (round to nearest even) copy of X, and zeroed tile counters
-__global__ void qgemm_prep_kernel(const float4 *__restrict__ x, uint2 *__restrict__ xb, long long n4,
-                                  unsigned int *cnt, int ncnt) {
+// Y of the split tiles: part sum in CTA order.  Block (tile, 8-column slice): thread = 4
+// consecutive rows of one column; whole tiles (written by their CTA) are skipped.
+__global__ void __launch_bounds__(256) qgemm_reduce_kernel(const GemmArgs a, int G) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tile = static_cast<int>(blockIdx.y);
+  const long long ts = static_cast<long long>(tile) * a.KS, te = ts + a.KS;
+  const int bf = range_owner(ts, a.total, G), bl = range_owner(te - 1, a.total, G);
+  if (bf == bl) return;  // one CTA held the whole tile
+  const int mt = tile / a.n_tt, tt = tile - mt * a.n_tt;
+  const int m4 = threadIdx.x & 31, col = static_cast<int>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int bp = bf; bp <= bl; ++bp) {
+    const long long sbp = range_start(bp, a.total, G);
+    if (sbp >= range_start(bp + 1, a.total, G)) continue;  // an empty range
+    const int sl = 2 * bp + (sbp < ts ? 1 : 0);
+    const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part + static_cast<size_t>(sl) * BT * BM) + col * (BM / 4) + m4);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  const int t = tt * BT + col, mg = mt * BM + 4 * m4;
+  if (t >= a.T) return;
+  float *yr = a.y + static_cast<size_t>(t) * a.M;
+  if (mg + 3 < a.M && (a.M & 3) == 0) {
+    *reinterpret_cast<float4 *>(yr + mg) = acc;
+  } else {
+    if (mg < a.M) yr[mg] = acc.x;
+    if (mg + 1 < a.M) yr[mg + 1] = acc.y;
+    if (mg + 2 < a.M) yr[mg + 2] = acc.z;
+    if (mg + 3 < a.M) yr[mg + 3] = acc.w;
+  }
+}
+
+// f32 -> bf16 (round to nearest even) copy of X
+__global__ void qgemm_prep_kernel(const float4 *__restrict__ x, uint2 *__restrict__ xb, long long n4) {
   pdl_wait();
   pdl_launch_dependents();
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -384,14 +339,12 @@ __global__ void qgemm_prep_kernel(const float4 *__restrict__ x, uint2 *__restric
       }
     }
   }
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < ncnt; i += stride)
-    cnt[i] = 0u;
 }
 
 struct GemmPlan {
   int n_mt, n_tt, KS, G;
   long long total;
-  size_t off_xb, off_cnt, off_part, bytes;
+  size_t off_xb, off_part, bytes;
 };
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t T, int sms) {
@@ -403,8 +356,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t T, int sms) {
   p.G = static_cast<int>(std::min<long long>(sms, p.total));
   auto up = [](size_t v) { return (v + 255) & ~static_cast<size_t>(255); };
   p.off_xb = 0;
-  p.off_cnt = up(static_cast<size_t>(T) * N * 2);
-  p.off_part = p.off_cnt + up(static_cast<size_t>(p.n_mt) * p.n_tt * 4);
+  p.off_part = up(static_cast<size_t>(T) * N * 2);
   p.bytes = p.off_part + static_cast<size_t>(2) * p.G * BT * BM * 4;
   return p;
 }
@@ -426,7 +378,6 @@ qg_status gemm_tc(const void *w, const float *x, float *y, int64_t M, int64_t N,
   if (ws_bytes < p.bytes) return QG_EWORKSPACE;
   uint8_t *wsb = static_cast<uint8_t *>(ws);
   __nv_bfloat16 *xb = reinterpret_cast<__nv_bfloat16 *>(wsb + p.off_xb);
-  unsigned int *cnt = reinterpret_cast<unsigned int *>(wsb + p.off_cnt);
   float *part = reinterpret_cast<float *>(wsb + p.off_part);
 
   auto enc = qg::encode_fn();
@@ -457,13 +408,12 @@ qg_status gemm_tc(const void *w, const float *x, float *y, int64_t M, int64_t N,
   const long long n4 = T * N / 4;
   const int pb = static_cast<int>(std::min<long long>(4LL * dev.sms, (n4 + 8 * 256 - 1) / (8 * 256)));
   if (qg::launch_pdl(qgemm_prep_kernel, dim3(std::max(pb, 1)), dim3(256), 0, s, reinterpret_cast<const float4 *>(x),
-                     reinterpret_cast<uint2 *>(xb), n4, cnt, p.n_mt * p.n_tt) != cudaSuccess)
+                     reinterpret_cast<uint2 *>(xb), n4) != cudaSuccess)
     return QG_ECUDA;
 
   GemmArgs a{};
   a.y = y;
   a.part = part;
-  a.cnt = cnt;
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.T = static_cast<int>(T);
@@ -473,6 +423,14 @@ qg_status gemm_tc(const void *w, const float *x, float *y, int64_t M, int64_t N,
   a.total = p.total;
   if (!qg::set_smem_attr(reinterpret_cast<const void *>(qgemm_q8_0_kernel), SMEM_BYTES)) return QG_ECUDA;
   if (qg::launch_pdl(qgemm_q8_0_kernel, dim3(p.G), dim3(NTHREADS), SMEM_BYTES, s, wmap, xmap, a) != cudaSuccess)
+    return QG_ECUDA;
+  // tiles whose k steps span several CTAs: their parts are summed by all SMs at once
+  const int tiles = p.n_mt * p.n_tt;
+  bool split = false;
+  for (int t = 0; t < tiles && !split; ++t)
+    split = range_owner(static_cast<long long>(t) * p.KS, p.total, p.G) !=
+            range_owner(static_cast<long long>(t + 1) * p.KS - 1, p.total, p.G);
+  if (split && qg::launch_pdl(qgemm_reduce_kernel, dim3(BT / 8, tiles), dim3(256), 0, s, a, p.G) != cudaSuccess)
     return QG_ECUDA;
   return cudaGetLastError() == cudaSuccess ? QG_OK : QG_ECUDA;
 }
