@@ -10,9 +10,12 @@
 //   gemm     persistent, warp-specialised like the prefill GEMM: raw Q8_0 expert rows come
 //            by TMA through 3-D tensor maps over the expert pool (slot is the third
 //            coordinate), converter warps decode them to bf16, one thread issues
-//            tcgen05.mma (M 128 weight rows, N 64 tokens, f32 in TMEM).  Gate/up tiles hold
-//            64 gate rows and the same 64 up rows, so the epilogue forms
-//            act = g / (1 + exp(-g)) * u in place; down tiles write dn rows of their pairs.
+//            tcgen05.mma (M 128 weight rows, N 64 tokens, f32 in TMEM), and four epilogue
+//            warps read one of two TMEM accumulators while the next tile's MMAs fill the
+//            other.  Gate/up tiles hold 64 gate rows and the same 64 up rows, so the epilogue
+//            forms act = g / (1 + exp(-g)) * u (or the GELU-tanh form) in place; down tiles
+//            write dn rows of their pairs.  Inside moe_layer the down step reuses the gate/up
+//            step's plan and the bf16 act rows its epilogue wrote in expert order.
 //   combine  x[t] = x[t] + sum_j w_j dn[t, j] in pick order (then the residual, as the pages
 //            order it)
 #include <cuda.h>

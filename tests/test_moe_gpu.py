@@ -95,6 +95,22 @@ def test_router_other_shapes(qg, oracle_lib, E, k):
         assert np.allclose(wts.sum(axis=1), 1.0, rtol=1e-6)
 
 
+@pytest.mark.parametrize("T,E,H", [(512, 128, 2048), (64, 200, 96), (77, 33, 3072)])
+def test_router_many_tiles_same_logits_as_one_tile_calls(qg, T, E, H):
+    """From four 16-token tiles on, the router stages each tile in shared memory and runs a share
+    of the experts over it; it sums every logit in the same order as the one-tile router, so the
+    logits (and picks and weights) equal those of calls of at most 16 tokens, bit for bit."""
+    k = min(8, E)
+    xn = gs.activations(T, H, seed=T + E, stream=14)
+    wr = gs.router_weights(E, H, seed=E)
+    ids, wts, lg = _route(qg, xn, wr, k)
+    for t0 in range(0, T, 16):
+        sub = xn[t0:t0 + 16]
+        ids1, wts1, lg1 = _route(qg, sub, wr, k)
+        assert np.array_equal(lg[t0:t0 + 16].view(np.uint32), lg1.view(np.uint32)), t0
+        assert np.array_equal(ids[t0:t0 + 16], ids1) and np.array_equal(wts[t0:t0 + 16], wts1), t0
+
+
 def test_router_ties_go_to_the_lowest_id(qg, oracle_lib):
     """Identical router rows give bit-identical logits: the lower expert id is picked first."""
     T, H, E, k = 4, 128, 12, 4
