@@ -333,6 +333,9 @@ QG_DEVICE int build_plan(const MoeArgs &a, int TT, const PlanSmem &p) {
     // topk_token, so picks and weights equal the standalone router's
     const int TE = a.T * a.E;
     for (int i = tid; i < TE; i += NW * 32) p.tk_lg[i] = __ldcg(a.logits + i);
+    // a rank that no expert takes (NaN logits tie with everything) leaves pick -1, which the
+    // id check below reports
+    for (int z = tid; z < P; z += NW * 32) p.tk_ids[z] = -1;
     __syncthreads();
     for (int i = tid; i < TE; i += NW * 32) {
       const int t = i / a.E, e = i - t * a.E;
@@ -348,10 +351,12 @@ QG_DEVICE int build_plan(const MoeArgs &a, int TT, const PlanSmem &p) {
     __syncthreads();
     for (int t = tid; t < a.T; t += NW * 32) {
       const float *lt = p.tk_lg + t * a.E;
-      const float lmax = lt[p.tk_ids[t * a.k]];
+      const int e0 = p.tk_ids[t * a.k];
+      const float lmax = e0 >= 0 ? lt[e0] : 0.f;
       float den = 0.f;
       for (int j = 0; j < a.k; ++j) {
-        const float ex = expf(lt[p.tk_ids[t * a.k + j]] - lmax);
+        const int ej = p.tk_ids[t * a.k + j];
+        const float ex = ej >= 0 ? expf(lt[ej] - lmax) : 0.f;
         den += ex;
         p.tk_w[t * a.k + j] = ex;
       }
@@ -957,6 +962,8 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
     for (int i = 0; i < NW * kMaxNS; ++i) mbar_init(&wbar[i], 1);
     fence_mbar_init();
   }
+  // a rank that no expert takes (NaN logits tie with everything) leaves pick -1, an invalid id
+  if (threadIdx.x < kMaxK) s_ids[threadIdx.x] = -1;
   __syncthreads();
 
   // ---- phase 0: router logits of experts blockIdx.x, + G, ..., summed by kRouterWarps warps
@@ -1045,8 +1052,9 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
   if (warp == 0) {
     // softmax over the picks: one exponential per lane, the denominator summed in pick order
     // (the router's order, so the weights are the standalone router's bit for bit)
-    const float lmax = s_l[s_ids[0]];
-    const float ex = lane < k ? expf(s_l[s_ids[lane]] - lmax) : 0.f;
+    const int e0 = s_ids[0], el = lane < k ? s_ids[lane] : -1;
+    const float lmax = e0 >= 0 ? s_l[e0] : 0.f;
+    const float ex = el >= 0 ? expf(s_l[el] - lmax) : 0.f;
     float den = 0.f;
     for (int j = 0; j < k; ++j) den += __shfl_sync(0xFFFFFFFFu, ex, j);
     const float wt = ex / den;

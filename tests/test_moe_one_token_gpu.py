@@ -217,3 +217,31 @@ def test_one_workspace_serves_every_token_count(qg, oracle_lib):
     torch.cuda.synchronize()
     i2, w2, _ = _route(qg, xn, wr, k)
     assert np.array_equal(ids.cpu().numpy(), i2) and np.array_equal(wts.cpu().numpy(), w2)
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_nan_router_input_leaves_no_pick_unset(qg, T):
+    """A NaN token row makes every router logit NaN, so every expert ranks first and ranks 1..k-1
+    have no expert: those picks come back -1 and the status word reports invalid ids, while the
+    call still completes (T = 1 ranks inside the one-token kernel, T = 4 inside the gate/up
+    kernel).  The other rows of the T = 4 call are finite and keep valid picks."""
+    H, F, E, k = 512, 96, 16, 4
+    ex = Experts(gs.Q8_0, E, H, F, seed=75)
+    gate, up, down = ex.bases()
+    wr = to_dev(gs.router_weights(E, H, seed=75), torch)
+    xn = gs.activations(T, H, seed=75, stream=63)
+    xn[0] = np.nan
+    ids = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    wts = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    act = torch.zeros((T * k, F), dtype=torch.float32, device="cuda")
+    x = to_dev(gs.activations(T, H, seed=75, stream=64), torch)
+    ws = _ws(qg, T, k, E, H, F)
+    qg.device_status()  # clear
+    qg.moe_layer(gs.Q8_0, to_dev(xn, torch), wr, gate, up, down, ex.stride, None, E, T, H, F, E, k, ids, wts, act, x,
+                 ws)
+    torch.cuda.synchronize()
+    assert qg.device_status() & (1 << qg.QG_EDEVICE_ID)
+    got = ids.cpu().numpy()
+    assert 0 <= got[0, 0] < E and (got[0, 1:] == -1).all(), got[0]
+    for t in range(1, T):
+        assert ((got[t] >= 0) & (got[t] < E)).all() and len(set(got[t])) == k, got[t]
