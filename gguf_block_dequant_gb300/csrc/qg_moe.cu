@@ -975,6 +975,11 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
   // so every CTA of a call reads the same count).
   pdl_wait();
   if (threadIdx.x == 0) s_misc[2] = static_cast<unsigned int>(ld_relaxed_u64(a.gen)) + 1u;
+  // hidden rows of phase 2 for this CTA; their residual values are read now (only this CTA
+  // writes them), so that the combine at the end does not wait for them
+  const int hA = static_cast<int>(static_cast<long long>(blockIdx.x) * H / G);
+  const int hB = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * H / G);
+  const float x_pre = threadIdx.x < hB - hA ? a.x[hA + threadIdx.x] : 0.f;
   __syncthreads();
   const unsigned int tag = s_misc[2];
   bool ok = true;
@@ -1095,10 +1100,8 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
       if (s_slot[j] < 0)
         for (int i = threadIdx.x; i < F; i += NW * 32) a.act[static_cast<size_t>(j) * F + i] = 0.f;
 
-  // hidden rows of phase 2 for this CTA (their down rows are requested right after each
-  // warp's gate/up items, into the ring slots the gate/up phase leaves free)
-  const int hA = static_cast<int>(static_cast<long long>(blockIdx.x) * H / G);
-  const int hB = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * H / G);
+  // the down rows of this CTA's hidden rows are requested right after each warp's gate/up
+  // items, into the ring slots the gate/up phase leaves free
 
   const uint32_t wo = static_cast<uint32_t>(D::woff(lane));
   uint32_t xo[D::NCH];
@@ -1288,7 +1291,7 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_one_token_kernel(const OneArgs
   for (int hl = threadIdx.x; hl < nh; hl += NW * 32) {
     float sum = 0.f;
     for (int jv = 0; jv < kv; ++jv) sum = fmaf(s_w[s_vz[jv]], part[hl * kMaxK + jv], sum);
-    if (ok) a.x[hA + hl] += sum;
+    if (ok) a.x[hA + hl] = (hl == static_cast<int>(threadIdx.x) ? x_pre : a.x[hA + hl]) + sum;
   }
   if (!ok) {
     if (lane == 0) moe_status(QG_STATUS_BIT_TIMEOUT);
