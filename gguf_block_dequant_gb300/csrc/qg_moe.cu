@@ -861,12 +861,13 @@ __global__ void __launch_bounds__(NW * 32, 1) moe_expert_kernel(const __grid_con
 // With a single token the layer is four short dependent steps (router, gate/up, down,
 // combine) around ~40 MB of weights, and separate launches spend most of the time on their
 // own start-up and drain.  This kernel runs them as phases of one persistent grid (one CTA
-// per SM, all co-resident: cooperative launch) separated by two grid barriers:
-//   phase 0  router logits, one expert row per CTA (its warps split the row);
-//   barrier
+// per SM, all co-resident: cooperative launch):
+//   phase 0  router logits, one expert row per CTA (its warps split the row), each published
+//            as a word tagged with the call; every CTA polls the E words until all carry the
+//            tag (no grid barrier);
 //   phase 1  every CTA ranks the logits itself (the same picks everywhere), then streams its
 //            share of the {gate i, up i} row pairs of the picked experts and writes
-//            act = silu(g) * u; meanwhile it asks L2 for the down rows it will need next;
+//            act = silu(g) * u; then it requests the down rows it will need next;
 //   barrier
 //   phase 2  every CTA owns a range of hidden rows h: it dots the down rows h of each picked
 //            expert with that expert's act row and adds sum_j w_j dn_j[h] to x[h] in pick
